@@ -1,0 +1,389 @@
+"""Throughput of the bf16 attention forward on one GB300, one JSON line.
+
+A step is one call of fa_fwd over the whole workload (default: B=1, H=32,
+N=16384, D=128, causal, the long-context throughput configuration), with the
+inputs already resident in device memory.  FLOPs per step = 4*D*P where P is
+the exact number of (query, key) pairs the mask allows (causal counts the
+lower triangle including the diagonal).  The inputs (Q, K, V: 384 MiB) are
+larger than the 126 MiB L2, so no flush is needed between timed steps.
+
+Also reported on the same line:
+  roofline      dominant kernel (the tcgen05 forward) against the measured
+                dense bf16 tensor peak; its duration is timed with CUDA events
+                on the launching stream;
+  e2e           the same metric through the C ABI with host buffers: every
+                step copies Q, K, V from pinned host memory, runs fa_fwd and
+                copies O and LSE back, all inside the timed region;
+  cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the same
+                workload on this host's cores (rank 0, N=1 only);
+  clocks        nvidia-smi SM clocks and throttle reasons sampled during the
+                timed region.
+
+--impl reference times the CPU oracle alone (the reference arm).
+Multi-GPU: one process per GPU under torchrun; the path shards by
+(batch, head) with no exchange, so every rank runs its own full workload
+(weak scaling) and rank 0 reports the units of all ranks over the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK_TFLOPS = 1900.0   # used only when MEASURED_PEAKS.json is absent
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_tiled_attention_23_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed loop runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- oracle
+_F32_CACHE = {}
+
+
+def oracle_sample(inp, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on randomly chosen query rows of the workload for
+    about `budget_s` seconds; returns (flops, seconds, rows, threads)."""
+    import oracle
+
+    w = inp.workload
+    lib = oracle.library()
+    threads = lib.max_threads()
+    if w.name not in _F32_CACHE:
+        _F32_CACHE[w.name] = tuple(np.ascontiguousarray(x.float().numpy()) for x in (inp.q, inp.k, inp.v))
+    qf, kf, vf = _F32_CACHE[w.name]
+    kv = None if inp.kv_len is None else inp.kv_len.numpy()
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.H * w.N
+
+    def flops_of(rows):
+        i = rows % w.N
+        b = rows // (w.N * w.H)
+        L = np.full(rows.shape, w.N) if kv is None else np.clip(kv[b], 0, w.N)
+        nk = np.minimum(L, i + 1) if w.causal else L
+        return float(4 * w.D * nk.sum())
+
+    # calibrate on a small batch, then run one batch sized to the budget
+    rows = rng.integers(0, total_rows, max(threads, 16))
+    t0 = time.perf_counter()
+    lib.attention_rows(qf, kf, vf, rows, causal=w.causal, scale=w.scale, kv_len=kv)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(min(total_rows, max(len(rows), len(rows) * budget_s / dt)))
+    rows = rng.integers(0, total_rows, n)
+    t0 = time.perf_counter()
+    lib.attention_rows(qf, kf, vf, rows, causal=w.causal, scale=w.scale, kv_len=kv)
+    dt = time.perf_counter() - t0
+    return flops_of(rows), dt, n, threads
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    inp = workloads.make(args.workload)
+    w = inp.workload
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(inp, budget_s=min(1.0, args.ref_step_seconds), seed=1)
+    t_all = 0.0
+    flops_all = 0.0
+    rows_all = 0
+    threads = 1
+    for s in range(args.steps):
+        f, dt, n, threads = oracle_sample(inp, budget_s=args.ref_step_seconds, seed=100 + s)
+        vals.append(f / dt / 1e12)
+        t_all += dt
+        flops_all += f
+        rows_all += n
+    value = flops_all / t_all / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_all / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_all} random query rows of {w.name} over {args.steps} steps "
+                                   f"(~{args.ref_step_seconds:.0f} s each), fp64 two-pass naive attention"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import exact_tiled_attention_23_gb300 as fa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    fa.build()
+    fa.load()
+    inp = workloads.make(args.workload)
+    w = inp.workload
+    B, H, N, D = w.B, w.H, w.N, w.D
+    pairs = workloads.unmasked_pairs(N, w.causal, None if inp.kv_len is None else inp.kv_len.tolist(), B, H)
+    flops = 4.0 * D * pairs
+
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    kv = inp.kv_len.to(dev) if inp.kv_len is not None else None
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    kv_ptr = kv.data_ptr() if kv is not None else None
+    fwd = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_fp32
+
+    def step():
+        st = fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                 B, H, N, D, w.causal, float("nan"), kv_ptr, sp)
+        if st != fa.FA_OK:
+            raise fa.FAError(st, "fa_fwd")
+
+    torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_device_status(sp) != fa.FA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # ---- timed region: K steps, events on the launching stream -------------
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            t_begin = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            t_begin.record(stream)
+            for s in range(args.steps):
+                starts[s].record(stream)
+                step()
+                ends[s].record(stream)
+            t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    kernel_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    if fa.fa_device_status(sp) != fa.FA_OK:
+        raise RuntimeError("device status not OK after the timed loop")
+    t_max = total_ms
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(t.item())
+    value = world * flops * args.steps / (t_max * 1e-3) / 1e12
+    avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                "peak_kind": f"{peak_kind} dense bf16 (burst)", "kernel": "fwd_bf16_kernel",
+                "flops_per_launch": flops}
+
+    # ---- e2e through the C ABI with host buffers ---------------------------
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        e2e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                step()
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1) / e2e_steps
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": e2e_steps}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        f, dt, n, threads = oracle_sample(inp, budget_s=args.cpu_seconds)
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n} random query rows of {w.name} ({dt:.1f} s), fp64 two-pass naive attention"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "causal": w.causal,
+                   "padded": w.padded, "flops_per_step": flops, "unmasked_pairs": pairs,
+                   "l2": "inputs (Q,K,V) larger than L2; no flush between steps",
+                   "parallelism": f"replicas x{world} (no exchange)"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=8.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        # the whole reference run (warm-up + timed samples) stays within ~4 minutes
+        args.ref_step_seconds = min(args.ref_step_seconds, 200.0 / (args.steps + args.warmup))
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+"""Exact tiled attention forward for GB300 -- Python binding of libfa.so.
+
+The functions named like the C ABI (``fa_fwd``, ``fa_fwd_fp32``,
+``fa_status_string``, ``fa_device_status``, ``fa_last_error_detail``) take
+raw device pointers and sizes exactly as declared in ``include/fa.h`` and only
+marshal arguments through ctypes.  ``forward()`` is the convenience call on
+torch tensors: it checks shapes, allocates O and LSE with torch, and calls the
+same entry points on the current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels; there is no other code path, and calling
+without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import _build
+
+__all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+           "FAError", "load", "library_path", "fa_fwd", "fa_fwd_fp32", "fa_status_string",
+           "fa_device_status", "fa_last_error_detail", "forward", "build"]
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        super().__init__(f"{what}: {fa_status_string(status)}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libfa.so in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def load():
+    """The loaded ctypes library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"the CUDA attention library is not built ({path}); "
+                               "run exact_tiled_attention_23_gb300.build() first")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fwd_args = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
+        lib.fa_fwd.argtypes = fwd_args
+        lib.fa_fwd.restype = i32
+        lib.fa_fwd_fp32.argtypes = fwd_args
+        lib.fa_fwd_fp32.restype = i32
+        lib.fa_status_string.argtypes = [i32]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_device_status.argtypes = [vp]
+        lib.fa_device_status.restype = i32
+        lib.fa_last_error_detail.argtypes = []
+        lib.fa_last_error_detail.restype = ctypes.c_uint32
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- raw C ABI
+def fa_fwd(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream) -> int:
+    """bf16 forward; pointers are integers (device addresses) or None."""
+    return int(load().fa_fwd(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)), float(scale),
+                             kv_len, stream))
+
+
+def fa_fwd_fp32(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream) -> int:
+    """fp32 forward; pointers are integers (device addresses) or None."""
+    return int(load().fa_fwd_fp32(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)), float(scale),
+                                  kv_len, stream))
+
+
+def fa_status_string(status: int) -> str:
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except RuntimeError:
+        return {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+                4: "FA_ERR_TIMEOUT"}.get(int(status), "FA_UNKNOWN_STATUS")
+
+
+def fa_device_status(stream) -> int:
+    return int(load().fa_device_status(stream))
+
+
+def fa_last_error_detail() -> int:
+    return int(load().fa_last_error_detail())
+
+
+# ---------------------------------------------------------------- torch call
+def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse=None,
+            return_lse: bool = True, stream=None):
+    """O, LSE = attention(q, k, v) for CUDA tensors of shape [B, H, N, D].
+
+    bf16 inputs use the tensor-core path (D in {64, 128}); fp32 inputs use the
+    fp32 path (D <= 256).  scale=None selects 1/sqrt(D).  kv_len: optional
+    int32 CUDA tensor [B] of key lengths.  Runs asynchronously on `stream`
+    (default: torch's current stream).
+    """
+    import torch
+
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all have shape [B, H, N, D]")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must share dtype bfloat16 or float32")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    kv_ptr = None
+    if kv_len is not None:
+        if kv_len.dtype != torch.int32 or not kv_len.is_cuda or kv_len.numel() != B:
+            raise ValueError("kv_len must be an int32 CUDA tensor with B entries")
+        kv_len = kv_len.contiguous()
+        kv_ptr = kv_len.data_ptr()
+    sc = float("nan") if scale is None else float(scale)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_fp32
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+            lse.data_ptr() if lse is not None else None, B, H, N, D, causal, sc, kv_ptr, sp)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd" if q.dtype == torch.bfloat16 else "fa_fwd_fp32")
+    return (out, lse) if return_lse else out
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)

@@ -1,0 +1,182 @@
+// fa_api.cu -- the C ABI of the attention library: argument checks, the TMA
+// tensor maps, and the kernel launches.  Declared in include/fa.h.
+//
+// Every check that can fail runs before any CUDA call, so a rejected call has
+// no side effect.  The library allocates no device memory.
+#include "fa.h"
+#include "fa_internal.h"
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+uint32_t g_last_detail = 0;
+
+// Default bounded-wait budget: far above any legitimate wait (one key block
+// takes microseconds), short enough that a stuck kernel ends on its own.
+uint64_t wait_limit_ns()
+{
+    static uint64_t v = [] {
+        const char *e = std::getenv("FA_WAIT_LIMIT_MS");
+        double ms = e ? std::atof(e) : 4000.0;
+        if (!(ms > 0)) ms = 4000.0;
+        return (uint64_t)(ms * 1e6);
+    }();
+    return v;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_common(const void *Q, const void *K, const void *V, const void *O, int B, int H,
+                       int N, int D)
+{
+    if (B < 0 || H < 0 || N < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)B * H * N;
+    if (rows == 0) return FA_OK;
+    if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
+    // element counts must stay addressable with 64-bit offsets and fit the grid
+    if (rows > (int64_t)1 << 40 || (int64_t)B * H > INT32_MAX) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+float resolve_scale(float scale, int D)
+{
+    if (std::isnan(scale) || !(scale > 0.f) || std::isinf(scale)) return 1.0f / std::sqrt((float)D);
+    return scale;
+}
+
+fa::FwdParams make_params(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                          int H, int N, int D, int causal, float scale, const int32_t *kv_len)
+{
+    fa::FwdParams p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.lse = LSE;
+    p.kv_len = kv_len;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.D = D;
+    p.causal = causal ? 1 : 0;
+    p.scale = resolve_scale(scale, D);
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.wait_limit_ns = wait_limit_ns();
+    return p;
+}
+
+// 3-D map over a contiguous [B*H, N, D] bf16 array: box = 64 columns x 128 rows
+// of one head, 128-byte swizzle, zero fill outside [0, N) so a box never reads
+// the next head's rows.
+bool encode_bf16_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int64_t D)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                 int N, int D, int causal, float scale, const int32_t *kv_len, void *stream)
+{
+    fa_status st = check_common(Q, K, V, O, B, H, N, D);
+    if (st != FA_OK) return st;
+    if ((int64_t)B * H * N == 0) return FA_OK;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
+    if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
+    if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+    // one work item covers 256 query rows of one head; the grid is 1-D
+    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+    const int64_t BH = (int64_t)B * H;
+    CUtensorMap tq, tk, tv;
+    if (!encode_bf16_map(&tq, Q, BH, N, D) || !encode_bf16_map(&tk, K, BH, N, D) ||
+        !encode_bf16_map(&tv, V, BH, N, D))
+        return FA_ERR_CUDA;
+    const fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
+    cudaError_t e = fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, float *LSE, int B,
+                      int H, int N, int D, int causal, float scale, const int32_t *kv_len,
+                      void *stream)
+{
+    fa_status st = check_common(Q, K, V, O, B, H, N, D);
+    if (st != FA_OK) return st;
+    if ((int64_t)B * H * N == 0) return FA_OK;
+    if (D > 256) return FA_ERR_UNSUPPORTED;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                          reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                          reinterpret_cast<uintptr_t>(LSE) | reinterpret_cast<uintptr_t>(kv_len);
+    if (mis & 3u) return FA_ERR_INVALID_ARG;
+    const int64_t blocks = (int64_t)B * H * (((int64_t)N + 3) / 4);
+    if (blocks > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
+    cudaError_t e = fa::launch_fwd_fp32(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+const char *fa_status_string(fa_status s)
+{
+    switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_UNKNOWN_STATUS";
+}
+
+fa_status fa_device_status(void *stream)
+{
+    uint32_t v = 0;
+    if (fa::read_and_clear_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (v) {
+        g_last_detail = v;
+        if (v & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
+    }
+    return FA_OK;
+}
+
+uint32_t fa_last_error_detail(void) { return g_last_detail; }
+
+}  // extern "C"

@@ -1,0 +1,470 @@
+// fa_fwd_bf16.cu -- bf16 attention forward on the Blackwell tensor cores.
+//
+// The loop is the tiled online-softmax forward of "vectorized-flash-
+// attention-kernel" (Core algorithm; Key design decisions 1-3) laid out for
+// one sm_103a SM:
+//
+//   * one CTA owns a work item = (batch*head, 256 query rows) split into two
+//     128-row query tiles; each tile's scores S = Q K_j^T and output O live in
+//     tensor memory (one TMEM lane per query row, fp32);
+//   * warp 0 streams Q once and K_j, V_j through a ring of shared-memory slots
+//     with TMA (128-byte swizzled boxes of 128 rows x 64 columns);
+//   * warp 1 issues every tcgen05.mma: S_i = Q_i K_j^T (both operands in
+//     shared memory) and O_i += P_i V_j (P_i read from tensor memory);
+//   * warps 4-7 and 8-11 run the online softmax of tile 0 and tile 1: each
+//     thread loads its row of S_i from TMEM, masks, updates the running max m
+//     and sum l, writes P_i = exp2(S*scale*log2e - m) as bf16 back into the
+//     same TMEM columns, and rescales O_i in TMEM when the max moved;
+//   * while one tile's softmax runs, the tensor core works on the other tile,
+//     so the two softmax warpgroups alternate with the MMAs.
+//
+// The rescale is skipped while the running max grows by at most 8 in log2
+// units: m then stays a (stale) common reference for l and O, which is exact
+// in real arithmetic, and P <= 2^8 stays well inside fp32/bf16 range.
+//
+// Causal key blocks that lie wholly after the item's last query row are never
+// loaded (Key design decisions 3); key blocks at or past the key length are
+// skipped too, and items whose key length is 0 write O = 0, LSE = -inf
+// without touching the tensor core ("js-flash-attention-tiled-online-softmax-
+// exactness", Root causes 2).
+//
+// Every mbarrier wait is bounded by a time budget; a wait that runs out sets
+// the library's device status word, raises a CTA-wide abort flag, and every
+// role then drains its in-flight copies / MMAs, frees tensor memory and exits.
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+
+__device__ uint32_t g_status;
+
+namespace {
+
+constexpr int BM = 128;          // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;          // keys per step
+constexpr int kThreads = 384;    // 12 warps
+constexpr int kFirstSoftmaxWarp = 4;
+
+template <int D>
+struct Layout {
+    static constexpr int kChunks = D / 64;            // 128-byte swizzle atoms per row
+    static constexpr int kChunkBytes = BM * 128;      // one 128 x 64 bf16 box
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kSlots = (D == 64) ? 8 : 4;  // K/V ring depth (K_j, V_j alternate)
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
+    static constexpr int kBarBytes = 512;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;   // + alignment slack
+    static constexpr uint32_t kTmemCols = 512;
+    // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 after it.
+    // P_i (bf16 pairs) overwrites the first 64 columns of S_i.
+    __device__ static constexpr uint32_t col_s(int i) { return (uint32_t)i * 128u; }
+    __device__ static constexpr uint32_t col_o(int i) { return 256u + (uint32_t)i * D; }
+    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert((1 + 2 * kSlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+// tcgen05 instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int a_mn_major, int b_mn_major)
+{
+    return (1u << 4)                      // accumulator format: f32
+         | (1u << 7)                      // A format: bf16
+         | (1u << 10)                     // B format: bf16
+         | ((uint32_t)a_mn_major << 15)
+         | ((uint32_t)b_mn_major << 16)
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;               // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;               // swizzle: 128 B
+    return d;
+}
+
+struct Abort {
+    volatile int *flag;
+};
+
+// Bounded wait on phase `parity` of `bar`.  Returns false when the budget ran
+// out (the status word records `site`) or, if `follow_abort`, as soon as
+// another thread of the CTA has aborted.
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                             uint32_t site, Abort ab, bool follow_abort = true)
+{
+    if (ptx::mbar_test(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (ptx::mbar_test(bar, parity)) return true;
+        if ((++spins & 63u) == 0) {
+            if (follow_abort && *ab.flag) return false;
+            if (ptx::globaltimer_ns() - t0 > limit_ns) {
+                atomicOr(&g_status, kStatusTimeout | (site << 8));
+                *ab.flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int q_pairs)
+{
+    using Lay = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
+    uint64_t *q_full = bars;
+    uint64_t *slot_full = bars + 1;
+    uint64_t *slot_empty = slot_full + Lay::kSlots;
+    uint64_t *s_full = slot_empty + Lay::kSlots;   // [2]
+    uint64_t *p_full = s_full + 2;                 // [2]
+    uint64_t *o_final = p_full + 2;                // [2]
+    uint64_t *mma_drain = o_final + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
+    int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
+    const Abort ab{abort_word};
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work item: heaviest causal items first --------------------------
+    const int64_t BH = p.B * p.H;
+    const int64_t item = blockIdx.x;
+    const int64_t pair = (int64_t)q_pairs - 1 - item / BH;
+    const int64_t bh = item % BH;
+    const int64_t b = bh / p.H;
+    const int64_t N = p.N;
+    const int64_t q0 = pair * (2 * BM);
+    int64_t L = N;
+    if (p.kv_len) {
+        L = p.kv_len[b];
+        L = L < 0 ? 0 : (L > N ? N : L);
+    }
+    const int64_t kv_end = p.causal ? (L < q0 + 2 * BM ? L : q0 + 2 * BM) : L;
+    const int n_kv = (int)((kv_end + BN - 1) / BN);
+
+    // ---- set-up -----------------------------------------------------------
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(q_full, 1);
+        for (int s = 0; s < Lay::kSlots; ++s) {
+            ptx::mbar_init(&slot_full[s], 1);
+            ptx::mbar_init(&slot_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&s_full[i], 1);
+            ptx::mbar_init(&p_full[i], 4 * 32);
+            ptx::mbar_init(&o_final[i], 1);
+        }
+        ptx::mbar_init(mma_drain, 1);
+        *abort_word = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, Lay::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0 && n_kv > 0) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::mbar_arrive_expect_tx(q_full, 2 * Lay::kTileBytes);
+            for (int i = 0; i < 2; ++i)
+                for (int c = 0; c < Lay::kChunks; ++c)
+                    ptx::tma_load_3d(smem + Lay::kQOff + i * Lay::kTileBytes + c * Lay::kChunkBytes,
+                                     &tm_q, q_full, c * 64, (int32_t)(q0 + i * BM), (int32_t)bh);
+            uint32_t issued_mask = 0, last_parity = 0;   // per slot, for the final drain
+            bool ok = true;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                for (int w = 0; w < 2; ++w) {
+                    const int idx = 2 * j + w;
+                    const int slot = idx % Lay::kSlots;
+                    const int round = idx / Lay::kSlots;
+                    if (round > 0 &&
+                        !wait_bounded(&slot_empty[slot], (round - 1) & 1, p.wait_limit_ns,
+                                      kSiteSlotEmpty, ab)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&slot_full[slot], Lay::kTileBytes);
+                    const CUtensorMap *tm = w ? &tm_v : &tm_k;
+                    for (int c = 0; c < Lay::kChunks; ++c)
+                        ptx::tma_load_3d(smem + Lay::kKVOff + slot * Lay::kTileBytes + c * Lay::kChunkBytes,
+                                         tm, &slot_full[slot], c * 64, (int32_t)(j * BN), (int32_t)bh);
+                    issued_mask |= 1u << slot;
+                    last_parity = (last_parity & ~(1u << slot)) | ((uint32_t)(round & 1) << slot);
+                }
+            }
+            // Drain: no copy may still be landing in shared memory at exit.
+            wait_bounded(q_full, 0, p.wait_limit_ns, kSiteDrain, ab, false);
+            for (int s = 0; s < Lay::kSlots; ++s)
+                if (issued_mask & (1u << s))
+                    wait_bounded(&slot_full[s], (last_parity >> s) & 1, p.wait_limit_ns, kSiteDrain,
+                                 ab, false);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0 && n_kv > 0) {
+            constexpr uint32_t idesc_qk = make_idesc(BM, BN, 0, 0);
+            constexpr uint32_t idesc_pv = make_idesc(BM, D, 0, 1);
+            const uint32_t q_base = ptx::smem_u32(smem + Lay::kQOff);
+            const uint32_t kv_base = ptx::smem_u32(smem + Lay::kKVOff);
+
+            auto issue_s = [&](int i, int slot) {
+                const uint32_t qa = q_base + i * Lay::kTileBytes;
+                const uint32_t ka = kv_base + slot * Lay::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * Lay::kChunkBytes + (k % 4) * 32;
+                    ptx::mma_ss(tmem + Lay::col_s(i), make_sdesc(qa + off, 16, 1024),
+                                make_sdesc(ka + off, 16, 1024), idesc_qk, k > 0);
+                }
+            };
+            auto issue_pv = [&](int i, int slot, uint32_t acc) {
+                const uint32_t va = kv_base + slot * Lay::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    ptx::mma_ts(tmem + Lay::col_o(i), tmem + Lay::col_s(i) + k * 8,
+                                make_sdesc(va + k * 2048, Lay::kChunkBytes, 1024), idesc_pv,
+                                (acc | (uint32_t)k) != 0);
+                }
+            };
+
+            bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
+                      wait_bounded(&slot_full[0], 0, p.wait_limit_ns, kSiteSlotFull, ab);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_s(0, 0);
+                ptx::mma_commit(&s_full[0]);
+                issue_s(1, 0);
+                ptx::mma_commit(&s_full[1]);
+                ptx::mma_commit(&slot_empty[0]);
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int idx_v = 2 * j + 1, slot_v = idx_v % Lay::kSlots;
+                const int idx_k = 2 * j + 2, slot_k = idx_k % Lay::kSlots;
+                const bool more = (j + 1 < n_kv);
+                if (!wait_bounded(&slot_full[slot_v], (idx_v / Lay::kSlots) & 1, p.wait_limit_ns,
+                                  kSiteSlotFull, ab) ||
+                    !wait_bounded(&p_full[0], j & 1, p.wait_limit_ns, kSitePFull, ab))
+                    break;
+                ptx::tc_fence_after();
+                issue_pv(0, slot_v, j > 0);
+                if (!more) ptx::mma_commit(&o_final[0]);
+                if (more) {
+                    if (!wait_bounded(&slot_full[slot_k], (idx_k / Lay::kSlots) & 1, p.wait_limit_ns,
+                                      kSiteSlotFull, ab))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_s(0, slot_k);
+                    ptx::mma_commit(&s_full[0]);
+                }
+                if (!wait_bounded(&p_full[1], j & 1, p.wait_limit_ns, kSitePFull, ab)) break;
+                ptx::tc_fence_after();
+                issue_pv(1, slot_v, j > 0);
+                ptx::mma_commit(&slot_empty[slot_v]);
+                if (!more) ptx::mma_commit(&o_final[1]);
+                if (more) {
+                    issue_s(1, slot_k);
+                    ptx::mma_commit(&s_full[1]);
+                    ptx::mma_commit(&slot_empty[slot_k]);
+                }
+            }
+            // Drain: every MMA this thread issued is complete before TMEM is
+            // freed (on the normal path o_final already covered them; after an
+            // abort some may still be in flight).
+            ptx::mma_commit(mma_drain);
+            wait_bounded(mma_drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
+        }
+    } else if (warp >= kFirstSoftmaxWarp) {
+        // ================= online softmax + epilogue =================
+        const int i = (warp - kFirstSoftmaxWarp) / 4;      // query tile of this warpgroup
+        const int quarter = warp & 3;                      // TMEM lanes 32*quarter ..
+        const int r_local = quarter * 32 + lane;
+        const int64_t row = q0 + i * BM + r_local;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + Lay::col_s(i);
+        const uint32_t tO = tmem + lane_off + Lay::col_o(i);
+        const int64_t lim = p.causal ? (L < row + 1 ? L : row + 1) : L;   // visible keys: j < lim
+        const float sl2 = p.scale_log2;
+
+        float m_ref = -INFINITY;   // running max of scale*log2e*S (possibly stale by <= 8)
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const bool got = wait_bounded(&s_full[i], j & 1, p.wait_limit_ns, kSiteSFull, ab);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t s_raw[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s_raw[c]);
+            ptx::tmem_wait_ld();
+
+            const int64_t vis = lim - (int64_t)j * BN;          // columns k < vis are visible
+            if (vis < BN) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (c * 32 + t >= vis) s_raw[c][t] = f2u(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int t = 0; t < 32; ++t) mx = fmaxf(mx, u2f(s_raw[c][t]));
+            const float m_new = fmaxf(m_ref, mx * sl2);
+            const bool need = m_new > m_ref + 8.f;
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2_approx(m_ref - m_new);
+                if (j > 0) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tO + c * 32, o);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = f2u(u2f(o[t]) * alpha);
+                        ptx::tmem_st32(tO + c * 32, o);
+                    }
+                }
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const float p0 = ptx::ex2_approx(fmaf(u2f(s_raw[c][2 * t]), sl2, -mref_use));
+                    const float p1 = ptx::ex2_approx(fmaf(u2f(s_raw[c][2 * t + 1]), sl2, -mref_use));
+                    sum += p0 + p1;
+                    pk[t] = ptx::pack_bf16x2(p0, p1);
+                }
+                ptx::tmem_st16(tS + c * 16, pk);
+            }
+            ptx::tmem_wait_st();
+            l += sum;
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&p_full[i]);
+        }
+
+        // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----------------
+        bool have = (n_kv > 0) && ok;
+        if (have) {
+            const bool got = wait_bounded(&o_final[i], 0, p.wait_limit_ns, kSiteOFinal, ab);
+            have = __all_sync(0xffffffffu, got);
+        }
+        if (have || n_kv == 0) {
+            ptx::tc_fence_after();
+            const bool empty = !(l > 0.f);
+            const float inv = empty ? 0.f : 1.f / l;
+            uint16_t *orow = static_cast<uint16_t *>(p.o) + (bh * N + row) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n_kv > 0) {
+                    ptx::tmem_ld32(tO + c * 32, o);
+                    ptx::tmem_wait_ld();
+                }
+                if (row < N) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        w[t] = empty ? 0u
+                                     : ptx::pack_bf16x2(u2f(o[2 * t]) * inv, u2f(o[2 * t + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                }
+            }
+            if (p.lse && row < N)
+                p.lse[bh * N + row] = empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+
+    // ---- teardown ----------------------------------------------------------
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                     const CUtensorMap &tv, cudaStream_t stream)
+{
+    using Lay = Layout<D>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Lay::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int q_pairs = (int)((p.N + 2 * BM - 1) / (2 * BM));
+    const int64_t items = p.B * p.H * (int64_t)q_pairs;
+    fwd_bf16_kernel<D><<<(unsigned)items, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_pairs);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                            const CUtensorMap &tm_v, cudaStream_t stream)
+{
+    if (p.D == 64) return launch_d<64>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 128) return launch_d<128>(p, tm_q, tm_k, tm_v, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out)
+{
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    uint32_t v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+        if (e != cudaSuccess) return e;
+    }
+    *out = v;
+    return cudaSuccess;
+}
+
+}  // namespace fa

@@ -1,0 +1,52 @@
+// fa_internal.h -- declarations shared by the host launcher and the kernels
+// of the attention library (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fa {
+
+// Device-side status word.  Kernels OR an error code into the low byte and
+// record the site of the first give-up in the upper bits; the host reads and
+// clears it in fa_device_status.
+enum : uint32_t {
+    kStatusTimeout = 0x1u,
+};
+
+// Site codes of the bounded waits (upper 24 bits of the status word).
+enum WaitSite : uint32_t {
+    kSiteQFull = 1,
+    kSiteSlotFull = 2,
+    kSiteSlotEmpty = 3,
+    kSiteSFull = 4,
+    kSitePFull = 5,
+    kSiteOFinal = 6,
+    kSiteDrain = 7,
+};
+
+// Arguments common to both forward kernels.  Pointers are device pointers.
+struct FwdParams {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *o;
+    float *lse;               // may be null
+    const int32_t *kv_len;    // may be null (= N)
+    int64_t B, H, N, D;
+    int causal;
+    float scale;              // natural-log scale applied to Q K^T
+    float scale_log2;         // scale * log2(e)
+    uint64_t wait_limit_ns;   // bounded-wait budget of every mbarrier wait
+};
+
+// Launchers (return the CUDA error of the launch).
+cudaError_t launch_fwd_fp32(const FwdParams &p, cudaStream_t stream);
+cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                            const CUtensorMap &tm_v, cudaStream_t stream);
+
+// Read-and-clear of the device status word (synchronises `stream` first).
+cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out);
+
+}  // namespace fa

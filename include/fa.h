@@ -1,0 +1,111 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention forward pass for GB300 (sm_103a).
+ *
+ * The library computes, for every batch b and head h,
+ *
+ *     O   = softmax(scale * Q K^T + mask) V
+ *     LSE = log-sum-exp of each row of (scale * Q K^T + mask), natural log
+ *
+ * block by block with the online-softmax running max m and running sum l,
+ * rescaled by exp(m_old - m_new) whenever a key block raises the max, and
+ * without ever writing the N x N score matrix to device memory
+ * ("vectorized-flash-attention-kernel", Core algorithm and Key design
+ * decisions 1-3; "FlashAttention" module F08, Paper).  The mask hides key j
+ * from query i when j >= kv_len[b] (key padding), and, if `causal`, when
+ * j > i ("kvRow > qRow -> -inf", Core algorithm step 2).
+ *
+ * Layout (all arguments): Q, K, V and O are contiguous row-major
+ * [B, H, N, D] arrays; LSE is a contiguous [B, H, N] float array; kv_len is
+ * an int32 array of B entries.  Every pointer is DEVICE memory owned by the
+ * caller; the library allocates no device memory, keeps no pointer after the
+ * call returns, and its only state is a device-side status word (see
+ * fa_device_status) and a cached driver entry point.
+ *
+ * Calls are asynchronous: they validate their arguments on the host, enqueue
+ * one kernel on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ * and return.  Results are ready when the stream reaches that point.  Input
+ * and output buffers must not overlap.
+ *
+ * Numerical contract:
+ *   - rows whose mask hides every key (kv_len[b] == 0) get O = +0.0 exactly
+ *     and LSE = -inf, never NaN ("js-flash-attention-tiled-online-softmax-
+ *     exactness", Root causes 2);
+ *   - query rows at or past kv_len[b] are still computed over the keys
+ *     j < kv_len[b] (padding hides keys, not queries);
+ *   - kv_len entries outside [0, N] are clamped to that range on the device.
+ */
+#ifndef EXACT_TILED_ATTENTION_FA_H
+#define EXACT_TILED_ATTENTION_FA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misalignment, overflow */
+    FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head dim, device)        */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed                   */
+    FA_ERR_TIMEOUT = 4        /* a bounded device-side wait gave up (fa_device_status) */
+} fa_status;
+
+/*
+ * fa_fwd -- bf16 attention forward on the tensor cores (tcgen05, TMEM, TMA).
+ *
+ *   Q, K, V  const bf16 [B,H,N,D] device pointers, 16-byte aligned.
+ *   O        bf16 [B,H,N,D] device pointer, 16-byte aligned; each element is
+ *            the fp32 result rounded to nearest-even.
+ *   LSE      float [B,H,N] device pointer, or NULL to skip it (the saved row
+ *            statistic a recomputing backward needs: "vectorized-flash-
+ *            attention-kernel", Key design decisions 4).
+ *   B, H, N  batch, heads, sequence length; any value >= 0.  B*H*N == 0
+ *            returns FA_OK without a launch.
+ *   D        head dimension: 64 or 128 (others give FA_ERR_UNSUPPORTED).
+ *   causal   nonzero: key j is hidden from query i when j > i.
+ *   scale    softmax scale; NaN or <= 0 selects the default 1/sqrt(D)
+ *            ("vectorized-flash-attention-kernel", Constructor options).
+ *   kv_len   const int32 [B] device pointer of key lengths, or NULL (= N).
+ *   stream   cudaStream_t to enqueue on.
+ *
+ * Accumulation is fp32 (scores, running sums, O); P is rounded to bf16 for
+ * the second product.  Returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED from
+ * host-side checks before anything is enqueued, FA_ERR_CUDA if the launch
+ * fails.
+ */
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                 int B, int H, int N, int D, int causal, float scale,
+                 const int32_t *kv_len, void *stream);
+
+/*
+ * fa_fwd_fp32 -- fp32 attention forward (fp32 multiply-add on the CUDA cores,
+ * no TF32).  Same argument meaning as fa_fwd with float Q, K, V, O; any head
+ * dimension 1 <= D <= 256; pointers need only float alignment.
+ */
+fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, float *LSE,
+                      int B, int H, int N, int D, int causal, float scale,
+                      const int32_t *kv_len, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fa_status_string(fa_status s);
+
+/*
+ * fa_device_status -- synchronise `stream`, then report and clear the
+ * device-side status word.  Returns FA_ERR_TIMEOUT if a kernel of this
+ * library gave up a bounded wait since the last call (its output is then
+ * undefined), FA_ERR_CUDA if synchronising failed, FA_OK otherwise.
+ */
+fa_status fa_device_status(void *stream);
+
+/*
+ * fa_last_error_detail -- the site code of the last device-side give-up that
+ * fa_device_status saw (0 if none): a diagnostic for bug reports.
+ */
+uint32_t fa_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_TILED_ATTENTION_FA_H */

@@ -1,0 +1,95 @@
+"""The C ABI library on the host: it builds, loads, exports every symbol that
+include/fa.h declares, and rejects bad arguments before touching a GPU.
+
+No call here reaches a CUDA API: every case returns from the host-side checks.
+"""
+import os
+import re
+import shutil
+
+import pytest
+
+import exact_tiled_attention_23_gb300 as fa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="CUDA toolkit not present")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_fwd_fp32", "fa_status_string", "fa_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "FA_OK"), (1, "FA_ERR_INVALID_ARG"), (2, "FA_ERR_UNSUPPORTED"),
+                       (3, "FA_ERR_CUDA"), (4, "FA_ERR_TIMEOUT")]:
+        assert fa.fa_status_string(code) == name
+    assert fa.fa_status_string(99) == "FA_UNKNOWN_STATUS"
+
+
+NAN = float("nan")
+P = 0x10000  # a 16-byte-aligned stand-in address; never dereferenced (checks fail first)
+
+
+@pytest.mark.parametrize("fn", [fa.fa_fwd, fa.fa_fwd_fp32])
+def test_empty_problem_is_a_no_op(lib, fn):
+    for (B, H, N) in [(0, 4, 16), (2, 0, 16), (2, 4, 0)]:
+        assert fn(None, None, None, None, None, B, H, N, 64, 1, NAN, None, None) == fa.FA_OK
+
+
+@pytest.mark.parametrize("fn", [fa.fa_fwd, fa.fa_fwd_fp32])
+def test_null_and_negative_arguments(lib, fn):
+    assert fn(None, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fn(P, P, P, None, None, 1, 1, 16, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fn(P, P, P, P, None, -1, 1, 16, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fn(P, P, P, P, None, 1, 1, -5, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fn(P, P, P, P, None, 1, 1, 16, 0, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_bf16_head_dims(lib):
+    for D in (16, 32, 96, 192, 256):
+        assert fa.fa_fwd(P, P, P, P, None, 1, 1, 16, D, 1, NAN, None, None) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fp32_head_dim_limit(lib):
+    assert fa.fa_fwd_fp32(P, P, P, P, None, 1, 1, 16, 257, 1, NAN, None, None) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_misaligned_pointers(lib):
+    assert fa.fa_fwd(P + 2, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd(P, P, P, P + 8, None, 1, 1, 16, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd(P, P, P, P, P + 2, 1, 1, 16, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, P + 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_fp32(P + 2, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_grid_overflow_is_rejected(lib):
+    # B*H*ceil(N/256) above 2^31-1 work items
+    assert fa.fa_fwd(P, P, P, P, None, 65536, 65536, 512, 64, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_forward_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)

@@ -1,0 +1,224 @@
+"""Parity of the CUDA path with the fp64 CPU oracle, through the C ABI.
+
+Tolerances.  bf16 path (bf16 inputs, fp32 accumulation, bf16 output):
+max |O - O_ref| <= 2e-2 and mean |O - O_ref| <= 2e-3 over every row that
+sees at least one key; LSE within 1e-3 + 1e-5*|LSE|.  fp32 path:
+max |O - O_ref| <= 1e-5 and |LSE - LSE_ref| <= 1e-5 * max(1, |LSE|).
+Rows that see no key must be exact +0.0 with LSE = -inf (bitwise checks).
+
+Small cases compare every element; the full-size workloads are run in the
+launch configuration the benchmark times and compared on sampled rows that
+the oracle computes one by one, plus properties checked on every row.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_23_gb300 as fa
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN = 2e-2, 2e-3
+FP32_MAX = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    fa.build()
+    fa.load()
+    oracle.library()
+
+
+def run_gpu(inp, scale=None, stream=None):
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    kv = inp.kv_len.cuda() if inp.kv_len is not None else None
+    o, lse = fa.forward(q, k, v, causal=inp.causal, scale=scale, kv_len=kv, stream=stream)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    return o, lse
+
+
+def visible_keys(inp, rows):
+    """Number of keys each flat row sees (0 = fully masked)."""
+    w = inp.workload
+    N, H = w.N, w.H
+    i = rows % N
+    b = rows // (N * H)
+    L = np.full(rows.shape, N) if inp.kv_len is None else np.clip(inp.kv_len.numpy()[b], 0, N)
+    return np.minimum(L, i + 1) if inp.causal else L
+
+
+def compare(inp, o_gpu, lse_gpu, rows=None, scale=None):
+    """Compare GPU outputs with the oracle on `rows` (flat indices) or all rows."""
+    w = inp.workload
+    B, H, N, D = w.B, w.H, w.N, w.D
+    qf, kf, vf = (x.float().numpy() for x in (inp.q, inp.k, inp.v))
+    kv = None if inp.kv_len is None else inp.kv_len.numpy()
+    sc = w.scale if scale is None else scale
+    if rows is None:
+        o_ref, lse_ref = oracle.attention(qf, kf, vf, causal=inp.causal, scale=sc, kv_len=kv)
+        o_ref = o_ref.reshape(-1, D)
+        lse_ref = lse_ref.reshape(-1)
+        rows = np.arange(B * H * N)
+    else:
+        rows = np.asarray(rows, dtype=np.int64)
+        o_ref, lse_ref = oracle.attention_rows(qf, kf, vf, rows, causal=inp.causal, scale=sc, kv_len=kv)
+    og = o_gpu.float().reshape(-1, D)[torch.as_tensor(rows, device=o_gpu.device)].cpu().numpy().astype(np.float64)
+    lg = lse_gpu.reshape(-1)[torch.as_tensor(rows, device=lse_gpu.device)].cpu().numpy().astype(np.float64)
+    nk = visible_keys(inp, rows)
+    live = nk > 0
+    assert np.all(np.isfinite(og)), "non-finite O"
+    # fully masked rows: exact +0.0, LSE = -inf
+    if np.any(~live):
+        dead = og[~live]
+        assert np.all(dead == 0.0) and not np.any(np.signbit(dead)), "masked rows not exact +0"
+        assert np.all(np.isneginf(lg[~live])), "masked rows' LSE not -inf"
+    assert np.all(np.isfinite(lg[live])), "non-finite LSE on a live row"
+    err = np.abs(og[live] - o_ref[live])
+    lerr = np.abs(lg[live] - lse_ref[live])
+    if w.dtype == "fp32":
+        assert err.max(initial=0) <= FP32_MAX, f"fp32 max err {err.max()}"
+        assert np.all(lerr <= 1e-5 * np.maximum(1.0, np.abs(lse_ref[live]))), f"fp32 LSE err {lerr.max()}"
+    else:
+        assert err.max(initial=0) <= BF16_MAX, f"bf16 max err {err.max()}"
+        assert (err.mean() if err.size else 0.0) <= BF16_MEAN, f"bf16 mean err {err.mean()}"
+        assert np.all(lerr <= 1e-3 + 1e-5 * np.abs(lse_ref[live])), f"bf16 LSE err {lerr.max()}"
+    return err.max(initial=0), (err.mean() if err.size else 0.0), lerr.max(initial=0)
+
+
+BF16_CASES = [
+    # B, H, N, D, causal, kv_len
+    (1, 1, 1, 64, True, None),
+    (1, 2, 2, 128, False, None),
+    (1, 2, 127, 64, True, None),
+    (2, 2, 128, 128, True, None),
+    (1, 3, 129, 64, False, None),
+    (2, 1, 255, 128, True, None),
+    (1, 2, 256, 64, True, None),
+    (1, 1, 257, 128, False, None),
+    (2, 2, 300, 64, True, [300, 1]),
+    (3, 2, 513, 128, True, [0, 513, 200]),
+    (2, 2, 640, 64, False, [17, 640]),
+    (1, 2, 1000, 128, True, [999]),
+    (2, 1, 1024, 128, False, [1024, 129]),
+    (1, 1, 2048, 64, True, None),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len", BF16_CASES)
+def test_bf16_small_cases(B, H, N, D, causal, kv_len):
+    inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=causal, seed=N + D, kv_len=kv_len)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_bf16_explicit_scale(D):
+    inp = workloads.make_case(2, 2, 384, D, dtype="bf16", causal=True, seed=7)
+    o, lse = run_gpu(inp, scale=0.3)
+    compare(inp, o, lse, scale=0.3)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_bf16_large_logits(D):
+    """Query rows scaled x30 and x-30: the running max jumps between key
+    blocks, so the O rescale path runs; results stay exact within tolerance."""
+    inp = workloads.make_case(1, 2, 768, D, dtype="bf16", causal=True, seed=11)
+    q = inp.q.float()
+    q[:, :, ::5] *= 30.0
+    q[:, :, 1::7] *= -30.0
+    inp.q = q.to(torch.bfloat16)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
+FP32_CASES = [
+    (1, 1, 1, 16, True, None),
+    (1, 2, 128, 64, True, None),
+    (2, 1, 33, 33, False, [33, 5]),
+    (1, 2, 300, 128, True, [0]),
+    (2, 2, 97, 256, False, [97, 0]),
+    (1, 1, 1000, 64, True, [700]),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len", FP32_CASES)
+def test_fp32_small_cases(B, H, N, D, causal, kv_len):
+    inp = workloads.make_case(B, H, N, D, dtype="fp32", causal=causal, seed=N * 3 + D, kv_len=kv_len)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
+def test_outputs_are_deterministic():
+    inp = workloads.make_case(2, 4, 777, 128, dtype="bf16", causal=True, seed=3, kv_len=[777, 400])
+    o1, l1 = run_gpu(inp)
+    o2, l2 = run_gpu(inp)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_side_stream_and_no_allocation():
+    """Runs on a non-default stream and allocates no device memory."""
+    inp = workloads.make_case(1, 4, 1024, 128, dtype="bf16", causal=True, seed=5)
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    fa.forward(q, k, v, out=out, lse=lse, stream=s)          # warm-up (module load)
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fa.forward(q, k, v, out=out, lse=lse, stream=s)
+    s.synchronize()
+    assert torch.cuda.memory_allocated() == before
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+    compare(inp, out, lse)
+
+
+# ------------------------------------------------------------ full workloads
+def sample_rows(inp, n_random=768, seed=0):
+    w = inp.workload
+    B, H, N = w.B, w.H, w.N
+    rng = np.random.default_rng(seed)
+    rows = set(rng.integers(0, B * H * N, n_random).tolist())
+    for b in range(B):
+        for h in (0, H - 1):
+            for i in (0, 1, 127, 128, 255, 256, N // 2, N - 2, N - 1):
+                if 0 <= i < N:
+                    rows.add((b * H + h) * N + i)
+    if inp.kv_len is not None:
+        for b in range(B):
+            L = int(inp.kv_len[b])
+            for i in (L - 1, L, L + 1):
+                if 0 <= i < N:
+                    rows.add((b * H) * N + i)
+    if inp.spiky is not None:
+        sp = torch.nonzero(inp.spiky.reshape(-1))[:, 0].numpy()
+        rows.update(rng.choice(sp, size=min(128, sp.size), replace=False).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_full_workload(name):
+    inp = workloads.make(name)
+    o, lse = run_gpu(inp)
+    w = inp.workload
+    # properties on every row
+    assert not torch.isnan(o).any() and not torch.isinf(o).any()
+    assert not torch.isnan(lse).any()
+    if inp.kv_len is not None:
+        for b in range(w.B):
+            if int(inp.kv_len[b]) == 0:
+                assert bool((o[b] == 0).all()) and not bool(torch.signbit(o[b].float()).any())
+                assert bool(torch.isneginf(lse[b]).all())
+    assert not torch.isneginf(lse).any() or inp.kv_len is not None
+    if w.B * w.H * w.N <= 4096:
+        compare(inp, o, lse)
+    else:
+        compare(inp, o, lse, rows=sample_rows(inp, seed=w.index))
