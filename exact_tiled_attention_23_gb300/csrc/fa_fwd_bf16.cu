@@ -186,6 +186,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Registers: the producer / MMA warpgroup needs few; the softmax
+    // warpgroups hold a 128-column score row each.  128*96 + 256*200 fits in
+    // the 384*168 registers the CTA is launched with.  Each setmaxnreg sits
+    // in the branch of the role it serves.
+    if (warp < kFirstSoftmaxWarp) {
+    ptx::regs_dec<96>();
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && n_kv > 0) {
@@ -300,7 +306,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ptx::mma_commit(mma_drain);
             wait_bounded(mma_drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
         }
-    } else if (warp >= kFirstSoftmaxWarp) {
+    }
+    } else {
+        ptx::regs_inc<200>();
         // ================= online softmax + epilogue =================
         const int i = (warp - kFirstSoftmaxWarp) / 4;      // query tile of this warpgroup
         const int quarter = warp & 3;                      // TMEM lanes 32*quarter ..
@@ -335,42 +343,72 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int t = 0; t < 32; ++t)
                         if (c * 32 + t >= vis) s_raw[c][t] = f2u(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max: eight independent 3-input max chains, then a short tree
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int a = 0; a < 8; ++a) mx8[a] = u2f(s_raw[0][a]);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) mx = fmaxf(mx, u2f(s_raw[c][t]));
+            for (int k = 8; k < 128; k += 16)
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+                    mx8[a] = ptx::max3(mx8[a], u2f(s_raw[(k + 2 * a) / 32][(k + 2 * a) % 32]),
+                                       u2f(s_raw[(k + 2 * a + 1) / 32][(k + 2 * a + 1) % 32]));
+            const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
+                                   fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_new = fmaxf(m_ref, mx * sl2);
             const bool need = m_new > m_ref + 8.f;
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2_approx(m_ref - m_new);
                 if (j > 0) {
+                    const uint64_t a2 = ptx::pack2(alpha, alpha);
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
                         ptx::tmem_ld32(tO + c * 32, o);
                         ptx::tmem_wait_ld();
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) o[t] = f2u(u2f(o[t]) * alpha);
+                        for (int t = 0; t < 16; ++t) {
+                            float lo, hi;
+                            ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])), a2), lo, hi);
+                            o[2 * t] = f2u(lo);
+                            o[2 * t + 1] = f2u(hi);
+                        }
                         ptx::tmem_st32(tO + c * 32, o);
                     }
                 }
                 l *= alpha;
                 m_ref = m_new;
             }
+            // p = 2^(S*scale*log2e - m): packed FMA, MUFU ex2, packed running sums
             const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float sum = 0.f;
+            const uint64_t t2 = ptx::pack2(sl2, sl2);
+            const uint64_t nm2 = ptx::pack2(-mref_use, -mref_use);
+            uint64_t acc2[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) acc2[a] = 0ull;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const float p0 = ptx::ex2_approx(fmaf(u2f(s_raw[c][2 * t]), sl2, -mref_use));
-                    const float p1 = ptx::ex2_approx(fmaf(u2f(s_raw[c][2 * t + 1]), sl2, -mref_use));
-                    sum += p0 + p1;
+                    float y0, y1;
+                    ptx::unpack2(ptx::fma2(ptx::pack2(u2f(s_raw[c][2 * t]), u2f(s_raw[c][2 * t + 1])), t2, nm2),
+                                 y0, y1);
+                    const float p0 = ptx::ex2_approx(y0);
+                    const float p1 = ptx::ex2_approx(y1);
+                    acc2[t & 3] = ptx::add2(acc2[t & 3], ptx::pack2(p0, p1));
                     pk[t] = ptx::pack_bf16x2(p0, p1);
                 }
                 ptx::tmem_st16(tS + c * 16, pk);
+            }
+            float sum;
+            {
+                float a0, a1, b0, b1, c0, c1, d0, d1;
+                ptx::unpack2(acc2[0], a0, a1);
+                ptx::unpack2(acc2[1], b0, b1);
+                ptx::unpack2(acc2[2], c0, c1);
+                ptx::unpack2(acc2[3], d0, d1);
+                sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
             }
             ptx::tmem_wait_st();
             l += sum;
@@ -399,9 +437,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (row < N) {
                     uint32_t w[16];
 #pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        w[t] = empty ? 0u
-                                     : ptx::pack_bf16x2(u2f(o[2 * t]) * inv, u2f(o[2 * t + 1]) * inv);
+                    for (int t = 0; t < 16; ++t) {
+                        float lo, hi;
+                        ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])),
+                                               ptx::pack2(inv, inv)), lo, hi);
+                        w[t] = empty ? 0u : ptx::pack_bf16x2(lo, hi);
+                    }
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                     for (int t = 0; t < 4; ++t)

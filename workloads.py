@@ -121,9 +121,13 @@ def draw(B: int, H: int, N: int, D: int, dtype: str, seed: int, *, padded: str =
     return q.to(td), k.to(td), v.to(td), lens, spiky
 
 
-def make(name: str) -> Inputs:
-    """Inputs of a named workload (see WORKLOADS)."""
+def make(name: str, heads: Optional[int] = None) -> Inputs:
+    """Inputs of a named workload (see WORKLOADS); `heads` overrides H (a
+    smaller copy of the same workload, e.g. for profiler captures)."""
     w = WORKLOADS[name]
+    if heads is not None and heads != w.H:
+        w = Workload(f"{w.name}_h{heads}", w.index, w.dtype, w.B, int(heads), w.N, w.D, w.causal,
+                     padded=w.padded, spiky_rows=w.spiky_rows, spike=w.spike, note=w.note)
     q, k, v, lens, spiky = draw(w.B, w.H, w.N, w.D, w.dtype, w.seed, padded=w.padded,
                                 spiky_rows=w.spiky_rows, spike=w.spike)
     return Inputs(w, q, k, v, lens, spiky)
