@@ -18,9 +18,10 @@
 //   * while one tile's softmax runs, the tensor core works on the other tile,
 //     so the two softmax warpgroups alternate with the MMAs.
 //
-// The rescale is skipped while the running max grows by at most 8 in log2
-// units: m then stays a (stale) common reference for l and O, which is exact
-// in real arithmetic, and P <= 2^8 stays well inside fp32/bf16 range.
+// The reference max is lazy: after the first key block it moves only when a
+// block's sum of p exceeds 2^64, so almost every block needs no max scan and
+// no O rescale; l and O always share the reference, which keeps the result
+// exact in real arithmetic, and P <= 2^64 stays far inside fp32/bf16 range.
 //
 // Causal key blocks that lie wholly after the item's last query row are never
 // loaded (Key design decisions 3); key blocks at or past the key length are
@@ -46,6 +47,10 @@ constexpr int BM = 128;          // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;          // keys per step
 constexpr int kThreads = 384;    // 12 warps
 constexpr int kFirstSoftmaxWarp = 4;
+// Largest block sum of p kept without a max scan: 2^64.  It bounds every p
+// by 2^64, so l <= N * 2^64 and |O| <= N * 2^64 * max|V| stay far below the
+// fp32/bf16 limit of ~2^128 for any N < 2^31 and max|V| < 2^30.
+constexpr float kLazyLimit = 18446744073709551616.f;
 
 template <int D>
 struct Layout {
@@ -343,23 +348,28 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int t = 0; t < 32; ++t)
                         if (c * 32 + t >= vis) s_raw[c][t] = f2u(-INFINITY);
             }
-            // row max: eight independent 3-input max chains, then a short tree
-            float mx8[8];
+            // Reference max m_ref.  The first key block sets it from the row
+            // max.  Later blocks reuse it without scanning for their max as
+            // long as the block's sum of p stays <= kLazyLimit, which bounds
+            // every p (l, P and O stay far from overflow); a block that
+            // exceeds that, or gives inf/NaN, scans its max, raises m_ref,
+            // rescales O and l by 2^(m_old - m_new) and recomputes P.  l and O
+            // always share m_ref, so the result is exact in real arithmetic.
+            auto raise_reference = [&]() {
+                float mx8[8];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) mx8[a] = u2f(s_raw[0][a]);
+                for (int a = 0; a < 8; ++a) mx8[a] = u2f(s_raw[0][a]);
 #pragma unroll
-            for (int k = 8; k < 128; k += 16)
+                for (int k = 8; k < 128; k += 16)
 #pragma unroll
-                for (int a = 0; a < 8; ++a)
-                    mx8[a] = ptx::max3(mx8[a], u2f(s_raw[(k + 2 * a) / 32][(k + 2 * a) % 32]),
-                                       u2f(s_raw[(k + 2 * a + 1) / 32][(k + 2 * a + 1) % 32]));
-            const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
-                                   fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_new = fmaxf(m_ref, mx * sl2);
-            const bool need = m_new > m_ref + 8.f;
-            if (__any_sync(0xffffffffu, need)) {
+                    for (int a = 0; a < 8; ++a)
+                        mx8[a] = ptx::max3(mx8[a], u2f(s_raw[(k + 2 * a) / 32][(k + 2 * a) % 32]),
+                                           u2f(s_raw[(k + 2 * a + 1) / 32][(k + 2 * a + 1) % 32]));
+                const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
+                                       fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float m_new = fmaxf(m_ref, mx * sl2);
                 const float alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2_approx(m_ref - m_new);
-                if (j > 0) {
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     const uint64_t a2 = ptx::pack2(alpha, alpha);
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
@@ -378,37 +388,44 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 l *= alpha;
                 m_ref = m_new;
-            }
-            // p = 2^(S*scale*log2e - m): packed FMA, MUFU ex2, packed running sums
-            const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            const uint64_t t2 = ptx::pack2(sl2, sl2);
-            const uint64_t nm2 = ptx::pack2(-mref_use, -mref_use);
-            uint64_t acc2[4];
+            };
+            // p = 2^(S*scale*log2e - m_ref): packed FMA, MUFU ex2, packed sums;
+            // P goes back over the first 64 columns of S as bf16 pairs.
+            auto exp_pass = [&]() -> float {
+                const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                const uint64_t t2 = ptx::pack2(sl2, sl2);
+                const uint64_t nm2 = ptx::pack2(-mref_use, -mref_use);
+                uint64_t acc2[4];
 #pragma unroll
-            for (int a = 0; a < 4; ++a) acc2[a] = 0ull;
+                for (int a = 0; a < 4; ++a) acc2[a] = 0ull;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    float y0, y1;
-                    ptx::unpack2(ptx::fma2(ptx::pack2(u2f(s_raw[c][2 * t]), u2f(s_raw[c][2 * t + 1])), t2, nm2),
-                                 y0, y1);
-                    const float p0 = ptx::ex2_approx(y0);
-                    const float p1 = ptx::ex2_approx(y1);
-                    acc2[t & 3] = ptx::add2(acc2[t & 3], ptx::pack2(p0, p1));
-                    pk[t] = ptx::pack_bf16x2(p0, p1);
+                    for (int t = 0; t < 16; ++t) {
+                        float y0, y1;
+                        ptx::unpack2(ptx::fma2(ptx::pack2(u2f(s_raw[c][2 * t]), u2f(s_raw[c][2 * t + 1])), t2, nm2),
+                                     y0, y1);
+                        const float p0 = ptx::ex2_approx(y0);
+                        const float p1 = ptx::ex2_approx(y1);
+                        acc2[t & 3] = ptx::add2(acc2[t & 3], ptx::pack2(p0, p1));
+                        pk[t] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st16(tS + c * 16, pk);
                 }
-                ptx::tmem_st16(tS + c * 16, pk);
-            }
-            float sum;
-            {
                 float a0, a1, b0, b1, c0, c1, d0, d1;
                 ptx::unpack2(acc2[0], a0, a1);
                 ptx::unpack2(acc2[1], b0, b1);
                 ptx::unpack2(acc2[2], c0, c1);
                 ptx::unpack2(acc2[3], d0, d1);
-                sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+                return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+            };
+            if (__any_sync(0xffffffffu, m_ref == -INFINITY)) raise_reference();
+            float sum = exp_pass();
+            if (__any_sync(0xffffffffu, !(sum <= kLazyLimit))) {
+                raise_reference();
+                ptx::tmem_wait_st();      // the first pass's P stores land before the new ones
+                sum = exp_pass();
             }
             ptx::tmem_wait_st();
             l += sum;

@@ -136,6 +136,23 @@ def test_bf16_large_logits(D):
     compare(inp, o, lse)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_bf16_growing_logits(D, causal):
+    """Key magnitudes ramp x1 -> x60 along the sequence and some query rows
+    are scaled x3: later key blocks keep raising the row max far above the
+    reference taken from earlier blocks, so the rescale path runs on many
+    blocks."""
+    inp = workloads.make_case(1, 2, 1024, D, dtype="bf16", causal=causal, seed=13)
+    ramp = torch.linspace(1.0, 60.0, 1024)[None, None, :, None]
+    inp.k = (inp.k.float() * ramp).to(torch.bfloat16)
+    q = inp.q.float()
+    q[:, :, ::3] *= 3.0
+    inp.q = q.to(torch.bfloat16)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
 FP32_CASES = [
     (1, 1, 1, 16, True, None),
     (1, 2, 128, 64, True, None),
