@@ -150,6 +150,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------ multi-rank
+def slowest_rank_ms(local_ms: float, world: int, device=None) -> float:
+    """Max over ranks of the timed region (each rank runs its own replica)."""
+    if world <= 1:
+        return float(local_ms)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, slowest_ms: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank does `steps` steps of `flops_per_step`
+    (weak scaling), all within the slowest rank's time."""
+    return world * flops_per_step * steps / (slowest_ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------- oracle
 _F32_CACHE = {}
 
@@ -294,12 +311,8 @@ def run_ours(args, rank, world, local):
     total_ms = sum(kernel_ms) if flush else t_begin.elapsed_time(t_end)
     if fa.fa_device_status(sp) != fa.FA_OK:
         raise RuntimeError("device status not OK after the timed loop")
-    t_max = total_ms
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(t.item())
-    value = world * flops * args.steps / (t_max * 1e-3) / 1e12
+    t_max = slowest_rank_ms(total_ms, world, dev)
+    value = job_throughput(flops, args.steps, t_max, world)
     avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
 
     peaks, peak_kind = measured_peaks()
