@@ -268,10 +268,22 @@ def run_ours(args, rank, world, local):
     sp = stream.cuda_stream
     kv_ptr = kv.data_ptr() if kv is not None else None
     fwd = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_fp32
+    splits = None
+    if args.splits is not None:
+        if w.dtype != "bf16":
+            raise SystemExit("--splits needs a bf16 workload")
+        splits = args.splits if args.splits > 0 else fa.fa_fwd_splitkv_auto_splits(B, H, N, D)
+        ws_bytes = fa.fa_fwd_splitkv_workspace_bytes(B, H, N, D, splits)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)   # outside the timed region
 
     def step():
-        st = fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                 B, H, N, D, w.causal, float("nan"), kv_ptr, sp)
+        if splits is not None:
+            st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   B, H, N, D, w.causal, float("nan"), kv_ptr, splits,
+                                   workspace.data_ptr(), ws_bytes, sp)
+        else:
+            st = fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     B, H, N, D, w.causal, float("nan"), kv_ptr, sp)
         if st != fa.FA_OK:
             raise fa.FAError(st, "fa_fwd")
 
@@ -388,12 +400,13 @@ def run_ours(args, rank, world, local):
                    "padded": w.padded, "flops_per_step": flops, "unmasked_pairs": pairs,
                    "l2": ("256 MiB write before every step (flush not timed)" if flush else
                           "inputs (Q,K,V) larger than L2; no flush between steps"),
-                   "parallelism": f"replicas x{world} (no exchange)"},
+                   "parallelism": f"replicas x{world} (no exchange)",
+                   "path": "fa_fwd" if splits is None else f"fa_fwd_splitkv (splits={splits})"},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if splits is not None else 1),
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -414,6 +427,8 @@ def main():
                     help="override the workload's head count (smaller profiling captures)")
     ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
                     help="write a 256 MiB buffer before every timed step (auto: when Q,K,V fit in 2x L2)")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="time the split-KV path with this many key ranges (0 = automatic)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

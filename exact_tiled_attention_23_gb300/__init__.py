@@ -20,13 +20,16 @@ from . import _build
 
 __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FAError", "load", "library_path", "fa_fwd", "fa_fwd_fp32", "fa_status_string",
-           "fa_device_status", "fa_last_error_detail", "forward", "build"]
+           "fa_device_status", "fa_last_error_detail", "fa_fwd_splitkv",
+           "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "FA_MAX_SPLITS",
+           "forward", "build"]
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
 FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
+FA_MAX_SPLITS = 64
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +73,13 @@ def load():
         lib.fa_device_status.restype = i32
         lib.fa_last_error_detail.argtypes = []
         lib.fa_last_error_detail.restype = ctypes.c_uint32
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, i32, vp,
+                                       ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv.restype = i32
+        lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_splitkv_auto_splits.argtypes = [i32, i32, i32, i32]
+        lib.fa_fwd_splitkv_auto_splits.restype = i32
         _lib = lib
         return lib
 
@@ -85,6 +95,21 @@ def fa_fwd_fp32(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream) -> i
     """fp32 forward; pointers are integers (device addresses) or None."""
     return int(load().fa_fwd_fp32(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)), float(scale),
                                   kv_len, stream))
+
+
+def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, num_splits, workspace,
+                   workspace_bytes, stream) -> int:
+    """Split-KV bf16 forward with a caller-provided device workspace."""
+    return int(load().fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)), float(scale),
+                                     kv_len, int(num_splits), workspace, int(workspace_bytes), stream))
+
+
+def fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits) -> int:
+    return int(load().fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits))
+
+
+def fa_fwd_splitkv_auto_splits(B, H, N, D) -> int:
+    return int(load().fa_fwd_splitkv_auto_splits(B, H, N, D))
 
 
 def fa_status_string(status: int) -> str:
@@ -105,13 +130,18 @@ def fa_last_error_detail() -> int:
 
 # ---------------------------------------------------------------- torch call
 def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse=None,
-            return_lse: bool = True, stream=None):
+            return_lse: bool = True, stream=None, splits=None, workspace=None):
     """O, LSE = attention(q, k, v) for CUDA tensors of shape [B, H, N, D].
 
     bf16 inputs use the tensor-core path (D in {64, 128}); fp32 inputs use the
     fp32 path (D <= 256).  scale=None selects 1/sqrt(D).  kv_len: optional
     int32 CUDA tensor [B] of key lengths.  Runs asynchronously on `stream`
     (default: torch's current stream).
+
+    splits: None for fa_fwd; an integer (0 = automatic) selects the split-KV
+    path (bf16 only), whose workspace is `workspace` (a CUDA tensor of at
+    least fa_fwd_splitkv_workspace_bytes bytes) or, if None, a torch
+    allocation made here.
     """
     import torch
 
@@ -139,6 +169,19 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    if splits is not None:
+        if q.dtype != torch.bfloat16:
+            raise ValueError("the split-KV path takes bf16 inputs")
+        need = fa_fwd_splitkv_workspace_bytes(B, H, N, D, int(splits))
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, H, N, D, causal, sc,
+                            kv_ptr, int(splits), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), sp)
+        if st != FA_OK:
+            raise FAError(st, "fa_fwd_splitkv")
+        return (out, lse) if return_lse else out
     fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_fp32
     st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
             lse.data_ptr() if lse is not None else None, B, H, N, D, causal, sc, kv_ptr, sp)

@@ -86,6 +86,9 @@ fa::FwdParams make_params(const void *Q, const void *K, const void *V, void *O, 
     p.scale = resolve_scale(scale, D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.wait_limit_ns = wait_limit_ns();
+    p.num_splits = 1;
+    p.part_o = nullptr;
+    p.part_lse = nullptr;
     return p;
 }
 
@@ -131,6 +134,62 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
         return FA_ERR_CUDA;
     const fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
     cudaError_t e = fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits)
+{
+    if (B < 0 || H < 0 || N < 0 || D <= 0 || num_splits < 0 || num_splits > FA_MAX_SPLITS) return 0;
+    if (num_splits == 0) num_splits = fa_fwd_splitkv_auto_splits(B, H, N, D);
+    return (size_t)num_splits * (size_t)B * (size_t)H * (size_t)N * ((size_t)D + 1) * sizeof(float);
+}
+
+int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D)
+{
+    (void)D;
+    if (B <= 0 || H <= 0 || N <= 0) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
+    // one CTA per SM (shared memory), so fill one wave without a ragged second
+    // one, and keep at least two key blocks in every range
+    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    const int64_t blocks = ((int64_t)N + 127) / 128;
+    int64_t s = items >= sms ? 1 : sms / items;
+    if (s > blocks / 2) s = blocks / 2;
+    if (s > FA_MAX_SPLITS) s = FA_MAX_SPLITS;
+    return s < 1 ? 1 : (int)s;
+}
+
+fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                         int H, int N, int D, int causal, float scale, const int32_t *kv_len,
+                         int num_splits, void *workspace, size_t workspace_bytes, void *stream)
+{
+    fa_status st = check_common(Q, K, V, O, B, H, N, D);
+    if (st != FA_OK) return st;
+    if ((int64_t)B * H * N == 0) return FA_OK;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (num_splits < 0 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
+    if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
+    if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+    if (num_splits == 0) num_splits = fa_fwd_splitkv_auto_splits(B, H, N, D);
+    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    if (items * num_splits > INT32_MAX) return FA_ERR_INVALID_ARG;
+    if (workspace_bytes < fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits)) return FA_ERR_INVALID_ARG;
+
+    const int64_t BH = (int64_t)B * H;
+    CUtensorMap tq, tk, tv;
+    if (!encode_bf16_map(&tq, Q, BH, N, D) || !encode_bf16_map(&tk, K, BH, N, D) ||
+        !encode_bf16_map(&tv, V, BH, N, D))
+        return FA_ERR_CUDA;
+    fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
+    p.num_splits = num_splits;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_lse = p.part_o + (size_t)num_splits * BH * N * D;
+    cudaError_t e = fa::launch_fwd_bf16_split(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

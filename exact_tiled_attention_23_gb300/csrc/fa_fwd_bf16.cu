@@ -126,7 +126,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uin
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-template <int D>
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int q_pairs)
@@ -151,8 +151,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int lane = threadIdx.x & 31;
 
     // ---- work item: heaviest causal items first --------------------------
+    // (split-KV: the num_splits CTAs of one item are adjacent and each takes a
+    // contiguous range of its key blocks)
     const int64_t BH = p.B * p.H;
-    const int64_t item = blockIdx.x;
+    const int splits = kSplit ? p.num_splits : 1;
+    const int64_t item = (int64_t)blockIdx.x / splits;
+    const int split = (int)((int64_t)blockIdx.x % splits);
     const int64_t pair = (int64_t)q_pairs - 1 - item / BH;
     const int64_t bh = item % BH;
     const int64_t b = bh / p.H;
@@ -164,7 +168,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         L = L < 0 ? 0 : (L > N ? N : L);
     }
     const int64_t kv_end = p.causal ? (L < q0 + 2 * BM ? L : q0 + 2 * BM) : L;
-    const int n_kv = (int)((kv_end + BN - 1) / BN);
+    const int n_all = (int)((kv_end + BN - 1) / BN);
+    const int blk0 = kSplit ? (int)((int64_t)n_all * split / splits) : 0;   // first key block of this CTA
+    const int n_kv = kSplit ? (int)((int64_t)n_all * (split + 1) / splits) - blk0 : n_all;
 
     // ---- set-up -----------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -225,7 +231,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const CUtensorMap *tm = w ? &tm_v : &tm_k;
                     for (int c = 0; c < Lay::kChunks; ++c)
                         ptx::tma_load_3d(smem + Lay::kKVOff + slot * Lay::kTileBytes + c * Lay::kChunkBytes,
-                                         tm, &slot_full[slot], c * 64, (int32_t)(j * BN), (int32_t)bh);
+                                         tm, &slot_full[slot], c * 64, (int32_t)((blk0 + j) * BN), (int32_t)bh);
                     issued_mask |= 1u << slot;
                     last_parity = (last_parity & ~(1u << slot)) | ((uint32_t)(round & 1) << slot);
                 }
@@ -340,7 +346,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s_raw[c]);
             ptx::tmem_wait_ld();
 
-            const int64_t vis = lim - (int64_t)j * BN;          // columns k < vis are visible
+            const int64_t vis = lim - (int64_t)(blk0 + j) * BN;   // columns k < vis are visible
             if (vis < BN) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -443,7 +449,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ptx::tc_fence_after();
             const bool empty = !(l > 0.f);
             const float inv = empty ? 0.f : 1.f / l;
-            uint16_t *orow = static_cast<uint16_t *>(p.o) + (bh * N + row) * D;
+            const float lse_row = empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
+            const int64_t flat = bh * N + row;
+            uint16_t *orow = static_cast<uint16_t *>(p.o) + flat * D;
+            float *prow = kSplit ? p.part_o + ((int64_t)split * BH * N + flat) * D : nullptr;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -453,24 +462,38 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 if (row < N) {
                     uint32_t w[16];
+                    float f[32];
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         float lo, hi;
                         ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])),
                                                ptx::pack2(inv, inv)), lo, hi);
+                        f[2 * t] = empty ? 0.f : lo;
+                        f[2 * t + 1] = empty ? 0.f : hi;
                         w[t] = empty ? 0u : ptx::pack_bf16x2(lo, hi);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    if (kSplit) {
+                        // normalised fp32 partial output of this key range
+                        float4 *dst = reinterpret_cast<float4 *>(prow + c * 32);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                        for (int t = 0; t < 8; ++t)
+                            dst[t] = make_float4(f[4 * t], f[4 * t + 1], f[4 * t + 2], f[4 * t + 3]);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                    }
                 }
             }
-            if (p.lse && row < N)
-                p.lse[bh * N + row] = empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
+            if (row < N) {
+                if (kSplit)
+                    p.part_lse[(int64_t)split * BH * N + flat] = lse_row;
+                else if (p.lse)
+                    p.lse[flat] = lse_row;
+            }
         }
     }
-
     // ---- teardown ----------------------------------------------------------
     ptx::tc_fence_before();
     __syncthreads();
@@ -480,22 +503,89 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D>
+template <int D, bool kSplit>
 cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                      const CUtensorMap &tv, cudaStream_t stream)
 {
     using Lay = Layout<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kSplit>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int q_pairs = (int)((p.N + 2 * BM - 1) / (2 * BM));
-    const int64_t items = p.B * p.H * (int64_t)q_pairs;
-    fwd_bf16_kernel<D><<<(unsigned)items, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_pairs);
+    const int64_t ctas = p.B * p.H * (int64_t)q_pairs * (kSplit ? p.num_splits : 1);
+    fwd_bf16_kernel<D, kSplit><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_pairs);
+    return cudaGetLastError();
+}
+
+// Merge of the split-KV partial states ("FlashAttention" module, Math: partial
+// softmax states merge associatively).  Partial s of a row carries its
+// normalised output O_s and LSE_s over its key range; with m = max_s LSE_s and
+// w_s = exp(LSE_s - m): O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s.
+// Ranges with no visible key have LSE_s = -inf and weight 0; a row with none
+// at all gets O = +0 and LSE = -inf.  One warp per row, D/32 columns per lane.
+template <int D>
+__global__ void __launch_bounds__(256)
+merge_splits_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
+                    uint16_t *__restrict__ out, float *__restrict__ lse, int64_t rows, int splits)
+{
+    constexpr int kPer = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float m = -INFINITY;
+    for (int s = 0; s < splits; ++s) m = fmaxf(m, part_lse[(int64_t)s * rows + row]);
+    float acc[kPer];
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    if (m > -INFINITY) {
+        for (int s = 0; s < splits; ++s) {
+            const float ls = part_lse[(int64_t)s * rows + row];
+            if (!(ls > -INFINITY)) continue;
+            const float w = expf(ls - m);
+            wsum += w;
+            const float *src = part_o + ((int64_t)s * rows + row) * D + lane * kPer;
+            if constexpr (kPer == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] = fmaf(w, v.x, acc[0]);
+                acc[1] = fmaf(w, v.y, acc[1]);
+                acc[2] = fmaf(w, v.z, acc[2]);
+                acc[3] = fmaf(w, v.w, acc[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                acc[0] = fmaf(w, v.x, acc[0]);
+                acc[1] = fmaf(w, v.y, acc[1]);
+            }
+        }
+    }
+    const bool empty = !(wsum > 0.f);
+    const float inv = empty ? 0.f : 1.f / wsum;
+    uint32_t packed[kPer / 2];
+#pragma unroll
+    for (int c = 0; c < kPer / 2; ++c)
+        packed[c] = empty ? 0u : ptx::pack_bf16x2(acc[2 * c] * inv, acc[2 * c + 1] * inv);
+    uint16_t *dst = out + row * D + lane * kPer;
+    if constexpr (kPer == 4)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    else
+        *reinterpret_cast<uint32_t *>(dst) = packed[0];
+    if (lse && lane == 0) lse[row] = empty ? -INFINITY : m + logf(wsum);
+}
+
+template <int D>
+cudaError_t launch_split(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, cudaStream_t stream)
+{
+    cudaError_t e = launch_d<D, true>(p, tq, tk, tv, stream);
+    if (e != cudaSuccess) return e;
+    const int64_t rows = p.B * p.H * p.N;
+    merge_splits_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        p.part_o, p.part_lse, static_cast<uint16_t *>(p.o), p.lse, rows, p.num_splits);
     return cudaGetLastError();
 }
 
@@ -504,8 +594,16 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, cudaStream_t stream)
 {
-    if (p.D == 64) return launch_d<64>(p, tm_q, tm_k, tm_v, stream);
-    if (p.D == 128) return launch_d<128>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 64) return launch_d<64, false>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 128) return launch_d<128, false>(p, tm_q, tm_k, tm_v, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                  const CUtensorMap &tm_v, cudaStream_t stream)
+{
+    if (p.D == 64) return launch_split<64>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 128) return launch_split<128>(p, tm_q, tm_k, tm_v, stream);
     return cudaErrorInvalidValue;
 }
 

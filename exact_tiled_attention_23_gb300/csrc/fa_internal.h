@@ -39,12 +39,22 @@ struct FwdParams {
     float scale;              // natural-log scale applied to Q K^T
     float scale_log2;         // scale * log2(e)
     uint64_t wait_limit_ns;   // bounded-wait budget of every mbarrier wait
+    // split-KV only: key blocks of every query item are divided into
+    // num_splits contiguous ranges; range s writes its normalised partial
+    // output part_o[s][B*H*N][D] (fp32) and part_lse[s][B*H*N].
+    int num_splits;
+    float *part_o;
+    float *part_lse;
 };
 
 // Launchers (return the CUDA error of the launch).
 cudaError_t launch_fwd_fp32(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, cudaStream_t stream);
+
+// Split-KV forward: partial kernel over key-block ranges, then the merge.
+cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                  const CUtensorMap &tm_v, cudaStream_t stream);
 
 // Read-and-clear of the device status word (synchronises `stream` first).
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out);

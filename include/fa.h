@@ -37,6 +37,7 @@
 #ifndef EXACT_TILED_ATTENTION_FA_H
 #define EXACT_TILED_ATTENTION_FA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -86,6 +87,44 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
 fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, float *LSE,
                       int B, int H, int N, int D, int causal, float scale,
                       const int32_t *kv_len, void *stream);
+
+/*
+ * Split-KV forward ("FlashAttention" module F08, Paper and Math: partial
+ * softmax states merge associatively).  Same computation and arguments as
+ * fa_fwd, for sequences too short to fill the GPU with query tiles: the key
+ * blocks of every (batch, head, 256-query-row) item are divided into
+ * `num_splits` contiguous ranges processed by separate CTAs.  Each range
+ * writes its normalised fp32 partial output and partial LSE to `workspace`,
+ * and a second kernel on the same stream merges them:
+ *     m = max_s LSE_s,  w_s = exp(LSE_s - m),
+ *     O = sum_s w_s O_s / sum_s w_s,  LSE = m + ln sum_s w_s.
+ * Ranges that see no key have LSE_s = -inf and weight 0.
+ *
+ *   num_splits       1..FA_MAX_SPLITS, or 0 for fa_fwd_splitkv_auto_splits().
+ *   workspace        caller-owned device memory, 16-byte aligned, of at least
+ *                    fa_fwd_splitkv_workspace_bytes(B,H,N,D,num_splits)
+ *                    bytes; its contents on entry do not matter, it is fully
+ *                    rewritten, and it must not be used by another call that
+ *                    may run at the same time.
+ * Returns FA_ERR_INVALID_ARG for a missing, misaligned or too small
+ * workspace or a split count out of range; otherwise as fa_fwd.
+ */
+#define FA_MAX_SPLITS 64
+
+fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                         int B, int H, int N, int D, int causal, float scale,
+                         const int32_t *kv_len, int num_splits, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace fa_fwd_splitkv needs: num_splits * B*H*N * (D + 1) * 4
+ * (0 for invalid sizes); num_splits 0 means the automatic choice. */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits);
+
+/* The split count fa_fwd_splitkv uses for num_splits = 0 on the current
+ * device: as many ranges as fill one wave of CTAs (one per SM) when there are
+ * fewer query items than SMs, at least two key blocks per range, at most
+ * FA_MAX_SPLITS. */
+int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *fa_status_string(fa_status s);

@@ -93,3 +93,24 @@ def test_forward_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.forward(q, q, q)
+
+
+def test_splitkv_workspace_size(lib):
+    # num_splits * B*H*N * (D + 1) floats
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 1024, 64, 3) == 3 * 2 * 8 * 1024 * 65 * 4
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 128, 1) == 129 * 4
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 1, 16, 64, fa.FA_MAX_SPLITS + 1) == 0
+    assert fa.fa_fwd_splitkv_workspace_bytes(-1, 1, 16, 64, 2) == 0
+
+
+def test_splitkv_argument_checks(lib):
+    big = 1 << 40
+    # missing / misaligned workspace, split count out of range, too small a workspace
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, 2, None, big, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, 2, P + 4, big, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, -1, P, big, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, fa.FA_MAX_SPLITS + 1, P, big, None) == fa.FA_ERR_INVALID_ARG
+    need = fa.fa_fwd_splitkv_workspace_bytes(1, 1, 16, 64, 2)
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, 2, P, need - 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 96, 1, NAN, None, 2, P, big, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_splitkv(None, None, None, None, None, 1, 1, 0, 64, 1, NAN, None, 2, None, 0, None) == fa.FA_OK

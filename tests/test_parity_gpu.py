@@ -153,6 +153,47 @@ def test_bf16_growing_logits(D, causal):
     compare(inp, o, lse)
 
 
+SPLIT_CASES = [
+    # B, H, N, D, causal, kv_len, splits
+    (1, 2, 1024, 64, False, None, 2),
+    (1, 2, 1024, 128, True, None, 3),
+    (2, 2, 777, 64, True, [777, 0], 4),
+    (2, 1, 300, 128, False, [1, 300], 2),
+    (1, 1, 2048, 128, True, [1500], 7),
+    (1, 3, 129, 64, True, None, 5),          # more ranges than key blocks: empty ranges
+    (2, 2, 1024, 64, False, None, 0),        # automatic split count
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len,splits", SPLIT_CASES)
+def test_bf16_splitkv(B, H, N, D, causal, kv_len, splits):
+    """Split-KV: partial states of key ranges merged associatively."""
+    inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=causal, seed=N + splits, kv_len=kv_len)
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    kv = inp.kv_len.cuda() if inp.kv_len is not None else None
+    o, lse = fa.forward(q, k, v, causal=causal, kv_len=kv, splits=splits)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    compare(inp, o, lse)
+    # the same result as the single-pass kernel within rounding of one bf16 step
+    o1, lse1 = fa.forward(q, k, v, causal=causal, kv_len=kv)
+    torch.cuda.synchronize()
+    assert (o.float() - o1.float()).abs().max().item() <= 2e-2
+    fin = torch.isfinite(lse1)
+    assert torch.equal(torch.isneginf(lse), torch.isneginf(lse1))
+    assert (lse[fin] - lse1[fin]).abs().max().item() <= 1e-4 if fin.any() else True
+
+
+@pytest.mark.parametrize("name", ["bf16_b2h8n1024d64_noncausal", "bf16_b2h8n1024d64_causal"])
+def test_splitkv_short_workloads(name):
+    inp = workloads.make(name)
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    o, lse = fa.forward(q, k, v, causal=inp.causal, splits=0)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    compare(inp, o, lse)
+
+
 FP32_CASES = [
     (1, 1, 1, 16, True, None),
     (1, 2, 128, 64, True, None),
