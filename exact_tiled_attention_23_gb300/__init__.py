@@ -22,6 +22,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "
            "FAError", "load", "library_path", "fa_fwd", "fa_fwd_fp32", "fa_status_string",
            "fa_device_status", "fa_last_error_detail", "fa_fwd_splitkv",
            "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "FA_MAX_SPLITS",
+           "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES",
            "forward", "build"]
 
 FA_OK = 0
@@ -30,6 +31,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_MAX_SPLITS = 64
+FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +82,9 @@ def load():
         lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_splitkv_auto_splits.argtypes = [i32, i32, i32, i32]
         lib.fa_fwd_splitkv_auto_splits.restype = i32
+        lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp,
+                                               i32, vp]
+        lib.fa_fwd_splitkv_noalloc.restype = i32
         _lib = lib
         return lib
 
@@ -102,6 +107,17 @@ def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, num_split
     """Split-KV bf16 forward with a caller-provided device workspace."""
     return int(load().fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)), float(scale),
                                      kv_len, int(num_splits), workspace, int(workspace_bytes), stream))
+
+
+def fa_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, num_splits,
+                           stream) -> int:
+    """Split-KV forward on the library's fixed device scratch, for callers
+    that cannot allocate device memory (no workspace argument; the call
+    allocates nothing).  Problems needing more than FA_NOALLOC_SCRATCH_BYTES
+    of scratch return FA_ERR_UNSUPPORTED.  Calls that overlap on the GPU
+    share the scratch and race."""
+    return int(load().fa_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)),
+                                             float(scale), kv_len, int(num_splits), stream))
 
 
 def fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits) -> int:

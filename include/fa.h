@@ -126,6 +126,42 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits
  * FA_MAX_SPLITS. */
 int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D);
 
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a library service.
+ *
+ * Some callers cannot call cudaMalloc or any allocator: code inside a
+ * framework's allocation-free region, a plugin that is only handed its input
+ * and output buffers, or a real-time loop where an allocation could block.
+ * This entry point takes no workspace.  It uses a fixed scratch array of
+ * FA_NOALLOC_SCRATCH_BYTES bytes that the library keeps in device memory.
+ * Every GPU that loads the library holds that array until the process exits.
+ * The call itself allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ * Arguments are those of fa_fwd_splitkv without the workspace.  The caller
+ * still passes the inputs and outputs.
+ *
+ * Limits and behaviour:
+ *   - A problem whose fa_fwd_splitkv_workspace_bytes(B,H,N,D,num_splits)
+ *     exceeds FA_NOALLOC_SCRATCH_BYTES is rejected with FA_ERR_UNSUPPORTED
+ *     before anything is enqueued.  Fewer splits, or fa_fwd, are the
+ *     alternatives.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current.  Make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, and it keeps the last call's contents.
+ *     Each call rewrites every part it reads, so nothing needs clearing.
+ *   - Two calls whose kernels overlap on the GPU (different streams, or
+ *     different host threads without ordering) race on the array and give
+ *     wrong results.  Order them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                 int B, int H, int N, int D, int causal, float scale,
+                                 const int32_t *kv_len, int num_splits, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *fa_status_string(fa_status s);
 
