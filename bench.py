@@ -254,7 +254,7 @@ def run_ours(args, rank, world, local):
         torch.distributed.init_process_group("nccl", device_id=dev)
     fa.build()
     fa.load()
-    inp = workloads.make(args.workload, heads=args.heads)
+    inp = workloads.make(args.workload, heads=args.heads, dtype=args.dtype)
     w = inp.workload
     B, H, N, D = w.B, w.H, w.N, w.D
     pairs = workloads.unmasked_pairs(N, w.causal, None if inp.kv_len is None else inp.kv_len.tolist(), B, H)
@@ -267,7 +267,7 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
     kv_ptr = kv.data_ptr() if kv is not None else None
-    fwd = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_fp32
+    fwd = {"bf16": fa.fa_fwd, "fp16": fa.fa_fwd_f16, "fp32": fa.fa_fwd_fp32}[w.dtype]
     splits = None
     if args.splits is not None:
         if w.dtype != "bf16":
@@ -329,7 +329,8 @@ def run_ours(args, rank, world, local):
 
     peaks, peak_kind = measured_peaks()
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
-    if w.dtype == "bf16":
+    if w.dtype in ("bf16", "fp16"):
+        # fp16 and bf16 have the same dense tensor rate (kind::f16)
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
@@ -427,6 +428,8 @@ def main():
                     help="override the workload's head count (smaller profiling captures)")
     ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
                     help="write a 256 MiB buffer before every timed step (auto: when Q,K,V fit in 2x L2)")
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
+                    help="override the element type of a 16-bit workload")
     ap.add_argument("--splits", type=int, default=None,
                     help="time the split-KV path with this many key ranges (0 = automatic)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -22,7 +22,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "
            "FAError", "load", "library_path", "fa_fwd", "fa_fwd_fp32", "fa_status_string",
            "fa_device_status", "fa_last_error_detail", "fa_fwd_splitkv",
            "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "FA_MAX_SPLITS",
-           "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES",
+           "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES", "fa_fwd_f16",
            "forward", "build"]
 
 FA_OK = 0
@@ -69,6 +69,8 @@ def load():
         lib.fa_fwd.restype = i32
         lib.fa_fwd_fp32.argtypes = fwd_args
         lib.fa_fwd_fp32.restype = i32
+        lib.fa_fwd_f16.argtypes = fwd_args
+        lib.fa_fwd_f16.restype = i32
         lib.fa_status_string.argtypes = [i32]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [vp]
@@ -94,6 +96,12 @@ def fa_fwd(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream) -> int:
     """bf16 forward; pointers are integers (device addresses) or None."""
     return int(load().fa_fwd(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)), float(scale),
                              kv_len, stream))
+
+
+def fa_fwd_f16(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream) -> int:
+    """fp16 forward on the tensor cores; pointers are integers (device addresses) or None."""
+    return int(load().fa_fwd_f16(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)), float(scale),
+                                 kv_len, stream))
 
 
 def fa_fwd_fp32(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream) -> int:
@@ -149,8 +157,8 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
             return_lse: bool = True, stream=None, splits=None, workspace=None):
     """O, LSE = attention(q, k, v) for CUDA tensors of shape [B, H, N, D].
 
-    bf16 inputs use the tensor-core path (D in {64, 128}); fp32 inputs use the
-    fp32 path (D <= 256).  scale=None selects 1/sqrt(D).  kv_len: optional
+    bf16 and fp16 inputs use the tensor-core path (D in {64, 128}); fp32
+    inputs use the fp32 path (D <= 256).  scale=None selects 1/sqrt(D).  kv_len: optional
     int32 CUDA tensor [B] of key lengths.  Runs asynchronously on `stream`
     (default: torch's current stream).
 
@@ -165,8 +173,9 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
         raise ValueError("q, k, v must all have shape [B, H, N, D]")
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors")
-    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("q, k, v must share dtype bfloat16 or float32")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float16,
+                                                              torch.float32):
+        raise ValueError("q, k, v must share dtype bfloat16, float16 or float32")
     q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     B, H, N, D = q.shape
     if out is None:
@@ -198,11 +207,11 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
         if st != FA_OK:
             raise FAError(st, "fa_fwd_splitkv")
         return (out, lse) if return_lse else out
-    fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_fp32
+    fn = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_f16, torch.float32: fa_fwd_fp32}[q.dtype]
     st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
             lse.data_ptr() if lse is not None else None, B, H, N, D, causal, sc, kv_ptr, sp)
     if st != FA_OK:
-        raise FAError(st, "fa_fwd" if q.dtype == torch.bfloat16 else "fa_fwd_fp32")
+        raise FAError(st, fn.__name__)
     return (out, lse) if return_lse else out
 
 

@@ -86,16 +86,18 @@ fa::FwdParams make_params(const void *Q, const void *K, const void *V, void *O, 
     p.scale = resolve_scale(scale, D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.wait_limit_ns = wait_limit_ns();
+    p.f16 = 0;
     p.num_splits = 1;
     p.part_o = nullptr;
     p.part_lse = nullptr;
     return p;
 }
 
-// 3-D map over a contiguous [B*H, N, D] bf16 array: box = 64 columns x 128 rows
-// of one head, 128-byte swizzle, zero fill outside [0, N) so a box never reads
-// the next head's rows.
-bool encode_bf16_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int64_t D)
+// 3-D map over a contiguous [B*H, N, D] array of 16-bit elements: box = 64
+// columns x 128 rows of one head, 128-byte swizzle, zero fill outside [0, N)
+// so a box never reads the next head's rows.
+bool encode_map16(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int64_t D,
+                  CUtensorMapDataType dtype)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -103,15 +105,51 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, in
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
     cuuint32_t box[3] = {64, 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+    CUresult r = fn(m, dtype, 3, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
+bool encode_bf16_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int64_t D)
+{
+    return encode_map16(m, base, BH, N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+// Shared checks and launch of the single-pass tensor-core kernel.
+fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                int N, int D, int causal, float scale, const int32_t *kv_len, void *stream, bool f16)
+{
+    fa_status st = check_common(Q, K, V, O, B, H, N, D);
+    if (st != FA_OK) return st;
+    if ((int64_t)B * H * N == 0) return FA_OK;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
+    if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
+    if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const int64_t BH = (int64_t)B * H;
+    const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv;
+    if (!encode_map16(&tq, Q, BH, N, D, dt) || !encode_map16(&tk, K, BH, N, D, dt) ||
+        !encode_map16(&tv, V, BH, N, D, dt))
+        return FA_ERR_CUDA;
+    fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
+    p.f16 = f16 ? 1 : 0;
+    cudaError_t e = fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status fa_fwd_f16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                     int N, int D, int causal, float scale, const int32_t *kv_len, void *stream)
+{
+    return fwd16(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream, true);
+}
 
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                  int N, int D, int causal, float scale, const int32_t *kv_len, void *stream)

@@ -1,4 +1,5 @@
-// fa_fwd_bf16.cu -- bf16 attention forward on the Blackwell tensor cores.
+// fa_fwd_bf16.cu -- bf16 (and fp16) attention forward on the Blackwell tensor
+// cores.
 //
 // The loop is the tiled online-softmax forward of "vectorized-flash-
 // attention-kernel" (Core algorithm; Key design decisions 1-3) laid out for
@@ -51,6 +52,8 @@ constexpr int kFirstSoftmaxWarp = 4;
 // by 2^64, so l <= N * 2^64 and |O| <= N * 2^64 * max|V| stay far below the
 // fp32/bf16 limit of ~2^128 for any N < 2^31 and max|V| < 2^30.
 constexpr float kLazyLimit = 18446744073709551616.f;
+// With fp16 operands P must also fit fp16 (max 65504): every p <= 2^15.
+constexpr float kLazyLimitF16 = 32768.f;
 
 template <int D>
 struct Layout {
@@ -73,12 +76,14 @@ struct Layout {
     static_assert((1 + 2 * kSlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
-// tcgen05 instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int a_mn_major, int b_mn_major)
+// tcgen05 instruction descriptor, kind::f16: A and B both bf16 (or both
+// f16), fp32 accumulator.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int a_mn_major, int b_mn_major,
+                                                  bool f16 = false)
 {
     return (1u << 4)                      // accumulator format: f32
-         | (1u << 7)                      // A format: bf16
-         | (1u << 10)                     // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)         // A format: f16 = 0, bf16 = 1
+         | ((f16 ? 0u : 1u) << 10)        // B format: same as A
          | ((uint32_t)a_mn_major << 15)
          | ((uint32_t)b_mn_major << 16)
          | ((uint32_t)(N >> 3) << 17)
@@ -126,7 +131,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uin
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-template <int D, bool kSplit>
+template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int q_pairs)
@@ -246,8 +251,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0 && n_kv > 0) {
-            constexpr uint32_t idesc_qk = make_idesc(BM, BN, 0, 0);
-            constexpr uint32_t idesc_pv = make_idesc(BM, D, 0, 1);
+            constexpr uint32_t idesc_qk = make_idesc(BM, BN, 0, 0, kF16);
+            constexpr uint32_t idesc_pv = make_idesc(BM, D, 0, 1, kF16);
             const uint32_t q_base = ptx::smem_u32(smem + Lay::kQOff);
             const uint32_t kv_base = ptx::smem_u32(smem + Lay::kKVOff);
 
@@ -415,7 +420,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const float p0 = ptx::ex2_approx(y0);
                         const float p1 = ptx::ex2_approx(y1);
                         acc2[t & 3] = ptx::add2(acc2[t & 3], ptx::pack2(p0, p1));
-                        pk[t] = ptx::pack_bf16x2(p0, p1);
+                        pk[t] = ptx::pack16x2<kF16>(p0, p1);
                     }
                     ptx::tmem_st16(tS + c * 16, pk);
                 }
@@ -428,7 +433,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             };
             if (__any_sync(0xffffffffu, m_ref == -INFINITY)) raise_reference();
             float sum = exp_pass();
-            if (__any_sync(0xffffffffu, !(sum <= kLazyLimit))) {
+            if (__any_sync(0xffffffffu, !(sum <= (kF16 ? kLazyLimitF16 : kLazyLimit)))) {
                 raise_reference();
                 ptx::tmem_wait_st();      // the first pass's P stores land before the new ones
                 sum = exp_pass();
@@ -470,7 +475,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                                ptx::pack2(inv, inv)), lo, hi);
                         f[2 * t] = empty ? 0.f : lo;
                         f[2 * t + 1] = empty ? 0.f : hi;
-                        w[t] = empty ? 0u : ptx::pack_bf16x2(lo, hi);
+                        w[t] = empty ? 0u : ptx::pack16x2<kF16>(lo, hi);
                     }
                     if (kSplit) {
                         // normalised fp32 partial output of this key range
@@ -503,14 +508,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool kSplit>
+template <int D, bool kSplit, bool kF16>
 cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                      const CUtensorMap &tv, cudaStream_t stream)
 {
     using Lay = Layout<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kSplit>,
+        cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, kSplit, kF16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
@@ -518,7 +523,7 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
     }
     const int q_pairs = (int)((p.N + 2 * BM - 1) / (2 * BM));
     const int64_t ctas = p.B * p.H * (int64_t)q_pairs * (kSplit ? p.num_splits : 1);
-    fwd_bf16_kernel<D, kSplit><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_pairs);
+    fwd_bf16_kernel<D, kSplit, kF16><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_pairs);
     return cudaGetLastError();
 }
 
@@ -528,7 +533,7 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
 // w_s = exp(LSE_s - m): O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s.
 // Ranges with no visible key have LSE_s = -inf and weight 0; a row with none
 // at all gets O = +0 and LSE = -inf.  One warp per row, D/32 columns per lane.
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
 merge_splits_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
                     uint16_t *__restrict__ out, float *__restrict__ lse, int64_t rows, int splits)
@@ -568,7 +573,7 @@ merge_splits_kernel(const float *__restrict__ part_o, const float *__restrict__ 
     uint32_t packed[kPer / 2];
 #pragma unroll
     for (int c = 0; c < kPer / 2; ++c)
-        packed[c] = empty ? 0u : ptx::pack_bf16x2(acc[2 * c] * inv, acc[2 * c + 1] * inv);
+        packed[c] = empty ? 0u : ptx::pack16x2<kF16>(acc[2 * c] * inv, acc[2 * c + 1] * inv);
     uint16_t *dst = out + row * D + lane * kPer;
     if constexpr (kPer == 4)
         *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
@@ -577,14 +582,14 @@ merge_splits_kernel(const float *__restrict__ part_o, const float *__restrict__ 
     if (lse && lane == 0) lse[row] = empty ? -INFINITY : m + logf(wsum);
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch_split(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, cudaStream_t stream)
 {
-    cudaError_t e = launch_d<D, true>(p, tq, tk, tv, stream);
+    cudaError_t e = launch_d<D, true, kF16>(p, tq, tk, tv, stream);
     if (e != cudaSuccess) return e;
     const int64_t rows = p.B * p.H * p.N;
-    merge_splits_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+    merge_splits_kernel<D, kF16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
         p.part_o, p.part_lse, static_cast<uint16_t *>(p.o), p.lse, rows, p.num_splits);
     return cudaGetLastError();
 }
@@ -594,16 +599,21 @@ cudaError_t launch_split(const FwdParams &p, const CUtensorMap &tq, const CUtens
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, cudaStream_t stream)
 {
-    if (p.D == 64) return launch_d<64, false>(p, tm_q, tm_k, tm_v, stream);
-    if (p.D == 128) return launch_d<128, false>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 64)
+        return p.f16 ? launch_d<64, false, true>(p, tm_q, tm_k, tm_v, stream)
+                     : launch_d<64, false, false>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 128)
+        return p.f16 ? launch_d<128, false, true>(p, tm_q, tm_k, tm_v, stream)
+                     : launch_d<128, false, false>(p, tm_q, tm_k, tm_v, stream);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                   const CUtensorMap &tm_v, cudaStream_t stream)
 {
-    if (p.D == 64) return launch_split<64>(p, tm_q, tm_k, tm_v, stream);
-    if (p.D == 128) return launch_split<128>(p, tm_q, tm_k, tm_v, stream);
+    if (p.f16) return cudaErrorInvalidValue;   // the split-KV path is bf16 only
+    if (p.D == 64) return launch_split<64, false>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 128) return launch_split<128, false>(p, tm_q, tm_k, tm_v, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -36,6 +36,7 @@ struct FwdParams {
     const int32_t *kv_len;    // may be null (= N)
     int64_t B, H, N, D;
     int causal;
+    int f16;                  // 16-bit operand type of the tensor-core path: 0 = bf16, 1 = fp16
     float scale;              // natural-log scale applied to Q K^T
     float scale_log2;         // scale * log2(e)
     uint64_t wait_limit_ns;   // bounded-wait budget of every mbarrier wait

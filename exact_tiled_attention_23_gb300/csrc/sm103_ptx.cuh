@@ -211,6 +211,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// Two fp32 values -> one f16x2 word (round to nearest even); `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The 16-bit pair of the operand type: f16 when kF16, else bf16.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi)
+{
+    if constexpr (kF16)
+        return pack_f16x2(lo, hi);
+    else
+        return pack_bf16x2(lo, hi);
+}
+
 }  // namespace ptx
 }  // namespace fa
 

@@ -80,6 +80,18 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
                  const int32_t *kv_len, void *stream);
 
 /*
+ * fa_fwd_f16 -- fp16 attention forward on the tensor cores ("FlashAttention"
+ * module F08, Exercises: the backward exercise's "fp16" variant of the same
+ * tiles).  Same arguments, layout and limits as fa_fwd with IEEE half Q, K,
+ * V and O (O rounded to nearest even); LSE stays fp32.  P is rounded to fp16
+ * for the second product; the reference max is raised whenever a key
+ * block's sum of p would pass 2^15, so P stays inside the fp16 range.
+ */
+fa_status fa_fwd_f16(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                     int B, int H, int N, int D, int causal, float scale,
+                     const int32_t *kv_len, void *stream);
+
+/*
  * fa_fwd_fp32 -- fp32 attention forward (fp32 multiply-add on the CUDA cores,
  * no TF32).  Same argument meaning as fa_fwd with float Q, K, V, O; any head
  * dimension 1 <= D <= 256; pointers need only float alignment.

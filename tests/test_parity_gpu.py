@@ -194,6 +194,34 @@ def test_splitkv_short_workloads(name):
     compare(inp, o, lse)
 
 
+F16_CASES = [
+    (1, 2, 127, 64, True, None),
+    (2, 2, 300, 128, False, [300, 0]),
+    (1, 2, 1024, 128, True, [1000]),
+    (2, 1, 513, 64, False, None),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len", F16_CASES)
+def test_f16_small_cases(B, H, N, D, causal, kv_len):
+    """fp16 operands: the same kernel with f16 MMA operands and an fp16 P."""
+    inp = workloads.make_case(B, H, N, D, dtype="fp16", causal=causal, seed=N + 5 * D, kv_len=kv_len)
+    o, lse = run_gpu(inp)
+    assert o.dtype == torch.float16
+    compare(inp, o, lse)
+
+
+def test_f16_large_logits():
+    """x30 query rows: the fp16 lazy limit (block sum 2^15) forces frequent
+    reference moves; P stays inside the fp16 range."""
+    inp = workloads.make_case(1, 2, 1024, 128, dtype="fp16", causal=True, seed=17)
+    q = inp.q.float()
+    q[:, :, ::4] *= 30.0
+    inp.q = q.to(torch.float16)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
 FP32_CASES = [
     (1, 1, 1, 16, True, None),
     (1, 2, 128, 64, True, None),

@@ -7,8 +7,8 @@ inputs without sharing any of the method's code.
 Every tensor is drawn on the CPU from ``torch.Generator('cpu')`` seeded with
 ``1234 + index`` (index = position of the workload below), in the order Q, K,
 V (standard normal, fp32), then any row-selection mask, then the per-batch
-key lengths.  Low-precision workloads round the fp32 draws to bf16 with
-round-to-nearest-even; the oracle reads those same rounded values upcast to
+key lengths.  Low-precision workloads round the fp32 draws to bf16 (or
+fp16) with round-to-nearest-even; the oracle reads those same rounded values upcast to
 fp32 (exact), so a measured error is the kernel's, not the input rounding's.
 """
 from __future__ import annotations
@@ -26,7 +26,7 @@ SEED_BASE = 1234
 class Workload:
     name: str
     index: int
-    dtype: str            # "fp32" or "bf16": the input / output element type
+    dtype: str            # "fp32", "bf16" or "fp16": the input / output element type
     B: int
     H: int
     N: int
@@ -87,7 +87,7 @@ class Inputs:
 
 
 def _torch_dtype(dtype: str):
-    return {"fp32": torch.float32, "bf16": torch.bfloat16}[dtype]
+    return {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
 
 
 def draw(B: int, H: int, N: int, D: int, dtype: str, seed: int, *, padded: str = "none",
@@ -121,12 +121,16 @@ def draw(B: int, H: int, N: int, D: int, dtype: str, seed: int, *, padded: str =
     return q.to(td), k.to(td), v.to(td), lens, spiky
 
 
-def make(name: str, heads: Optional[int] = None) -> Inputs:
+def make(name: str, heads: Optional[int] = None, dtype: Optional[str] = None) -> Inputs:
     """Inputs of a named workload (see WORKLOADS); `heads` overrides H (a
-    smaller copy of the same workload, e.g. for profiler captures)."""
+    smaller copy of the same workload, e.g. for profiler captures) and
+    `dtype` the element type of a 16-bit workload ("bf16" or "fp16")."""
     w = WORKLOADS[name]
-    if heads is not None and heads != w.H:
-        w = Workload(f"{w.name}_h{heads}", w.index, w.dtype, w.B, int(heads), w.N, w.D, w.causal,
+    if (heads is not None and heads != w.H) or (dtype is not None and dtype != w.dtype):
+        H = w.H if heads is None else int(heads)
+        dt = w.dtype if dtype is None else dtype
+        suffix = (f"_h{H}" if H != w.H else "") + (f"_{dt}" if dt != w.dtype else "")
+        w = Workload(f"{w.name}{suffix}", w.index, dt, w.B, H, w.N, w.D, w.causal,
                      padded=w.padded, spiky_rows=w.spiky_rows, spike=w.spike, note=w.note)
     q, k, v, lens, spiky = draw(w.B, w.H, w.N, w.D, w.dtype, w.seed, padded=w.padded,
                                 spiky_rows=w.spiky_rows, spike=w.spike)
