@@ -254,7 +254,7 @@ def run_ours(args, rank, world, local):
         torch.distributed.init_process_group("nccl", device_id=dev)
     fa.build()
     fa.load()
-    inp = workloads.make(args.workload, heads=args.heads, dtype=args.dtype)
+    inp = workloads.make(args.workload, heads=args.heads, dtype=args.dtype, seq=args.seq)
     w = inp.workload
     B, H, N, D = w.B, w.H, w.N, w.D
     pairs = workloads.unmasked_pairs(N, w.causal, None if inp.kv_len is None else inp.kv_len.tolist(), B, H)
@@ -428,6 +428,8 @@ def main():
                     help="override the workload's head count (smaller profiling captures)")
     ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
                     help="write a 256 MiB buffer before every timed step (auto: when Q,K,V fit in 2x L2)")
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override the workload's sequence length N (IO probe, profiler captures)")
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
                     help="override the element type of a 16-bit workload")
     ap.add_argument("--splits", type=int, default=None,
