@@ -9,8 +9,9 @@ Two independent implementations live here:
 
 * ``naive_attention.c`` -- plain fp64 two-pass attention over every allowed
   key of a row (the "standard attention" / "naive full-softmax reference" of
-  the pages).  This is THE oracle.  ``attention()`` and ``attention_rows()``
-  below call it through ctypes.
+  the pages), and its backward pass by recomputation.  This is THE oracle.
+  ``attention()``, ``attention_rows()`` and ``attention_bwd()`` below call
+  it through ctypes.
 * ``tiled.py`` -- the pages' block-tiled online-softmax loop in fp64 NumPy,
   plus the associative merge of partial softmax states.  It exists to pin the
   oracle (method equivalence at many block sizes) and is never compared with
@@ -75,6 +76,9 @@ class OracleLibrary:
                                               ctypes.c_int, ctypes.c_double, i32p,
                                               i64p, i64, f64p, f64p, ctypes.c_int]
         lib.oracle_attention_rows.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [f32p, f32p, f32p, f32p, f64p, f64p, f64p, i64, i64, i64,
+                                             i64, ctypes.c_int, ctypes.c_double, i32p, ctypes.c_int]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         self.lib = lib
@@ -142,6 +146,27 @@ class OracleLibrary:
         return o, lse
 
 
+    def attention_bwd(self, q, k, v, do, causal=True, scale=None, kv_len=None, threads=0):
+        """Gradients (dQ, dK, dV), fp64 [B,H,N,D], of sum(O * dO) for O = attention(q,k,v)."""
+        q, qp = self._f32(q)
+        k, kp = self._f32(k)
+        v, vp = self._f32(v)
+        do, dop = self._f32(do)
+        B, H, N, D = q.shape
+        if k.shape != q.shape or v.shape != q.shape or do.shape != q.shape:
+            raise ValueError("q, k, v, do must share the shape [B,H,N,D]")
+        scale = default_scale(D) if scale is None else float(scale)
+        kv, kvp = self._kv(kv_len, B)
+        dq, dk, dv = (np.empty((B, H, N, D), dtype=np.float64) for _ in range(3))
+        d64 = ctypes.POINTER(ctypes.c_double)
+        rc = self.lib.oracle_attention_bwd(qp, kp, vp, dop, dq.ctypes.data_as(d64), dk.ctypes.data_as(d64),
+                                           dv.ctypes.data_as(d64), B, H, N, D, int(bool(causal)), scale,
+                                           kvp, int(threads))
+        if rc != 0:
+            raise RuntimeError("oracle_attention_bwd failed")
+        return dq, dk, dv
+
+
 def default_scale(D: int) -> float:
     """softmaxScale default of the pages' constructor: 1/sqrt(d)."""
     return 1.0 / math.sqrt(D)
@@ -158,6 +183,11 @@ def library() -> OracleLibrary:
 
 def attention(q, k, v, causal=True, scale=None, kv_len=None, threads=0):
     return library().attention(q, k, v, causal=causal, scale=scale, kv_len=kv_len, threads=threads)
+
+
+def attention_bwd(q, k, v, do, causal=True, scale=None, kv_len=None, threads=0):
+    return library().attention_bwd(q, k, v, do, causal=causal, scale=scale, kv_len=kv_len,
+                                   threads=threads)
 
 
 def attention_rows(q, k, v, rows, causal=True, scale=None, kv_len=None, threads=0):

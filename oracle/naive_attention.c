@@ -179,3 +179,120 @@ int oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * Backward pass of the same attention, by recomputation ("FlashAttention"
+ * module F08, Math: backward pass via recomputation and the identity
+ * rowsum(dP * P) = rowsum(dO * O); "vectorized-flash-attention-kernel", Key
+ * design decisions 4: the saved row statistics let the backward rebuild P).
+ *
+ * For one (b, h), with P the masked softmax of scale * Q K^T (rows with no
+ * visible key are all zero), O = P V and an upstream gradient dO:
+ *
+ *   dV    = P^T dO
+ *   dP    = dO V^T
+ *   Delta = rowsum(dO * O)            (= rowsum(dP * P))
+ *   dS    = P * (dP - Delta)          (elementwise, row-broadcast Delta)
+ *   dQ    = scale * dS K
+ *   dK    = scale * dS^T Q
+ *
+ * Plain fp64, one head per OpenMP iteration, O(N) scratch per query row plus
+ * the head's fp64 accumulators for dK and dV.  Inputs are float32 arrays
+ * holding the exact values the GPU sees; outputs fp64 [B,H,N,D].
+ */
+static void oracle_bwd_head(const float *Q, const float *K, const float *V, const float *dO,
+                            double *dQ, double *dK, double *dV, int64_t N, int64_t D,
+                            int64_t head, int64_t L, int causal, double scale, double *p,
+                            double *dp, double *o)
+{
+    const int64_t base = head * N * D;
+    for (int64_t t = 0; t < N * D; ++t) {
+        dQ[base + t] = 0.0;
+        dK[base + t] = 0.0;
+        dV[base + t] = 0.0;
+    }
+    for (int64_t i = 0; i < N; ++i) {
+        int64_t n_vis = L;
+        if (causal && i + 1 < n_vis) n_vis = i + 1;
+        if (n_vis <= 0) continue;                 /* P row is zero: no gradient */
+        const float *q = Q + base + i * D;
+        const float *g = dO + base + i * D;
+        /* P row: two passes as in the forward definition */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < n_vis; ++j) {
+            const float *k = K + base + j * D;
+            double qk = 0.0;
+            for (int64_t d = 0; d < D; ++d) qk += (double)q[d] * (double)k[d];
+            p[j] = scale * qk;
+            if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < n_vis; ++j) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        for (int64_t j = 0; j < n_vis; ++j) p[j] /= l;
+        /* O row and Delta = rowsum(dO * O) */
+        for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+        for (int64_t j = 0; j < n_vis; ++j) {
+            const float *v = V + base + j * D;
+            for (int64_t d = 0; d < D; ++d) o[d] += p[j] * (double)v[d];
+        }
+        double delta = 0.0;
+        for (int64_t d = 0; d < D; ++d) delta += (double)g[d] * o[d];
+        /* dP row = dO_i . V_j, dS row = P * (dP - Delta) */
+        for (int64_t j = 0; j < n_vis; ++j) {
+            const float *v = V + base + j * D;
+            double s = 0.0;
+            for (int64_t d = 0; d < D; ++d) s += (double)g[d] * (double)v[d];
+            dp[j] = p[j] * (s - delta);
+        }
+        /* accumulate dV += P^T dO, dQ = scale dS K, dK += scale dS^T Q */
+        for (int64_t j = 0; j < n_vis; ++j) {
+            const float *k = K + base + j * D;
+            double *dvj = dV + base + j * D;
+            double *dkj = dK + base + j * D;
+            double *dqi = dQ + base + i * D;
+            for (int64_t d = 0; d < D; ++d) {
+                dvj[d] += p[j] * (double)g[d];
+                dqi[d] += scale * dp[j] * (double)k[d];
+                dkj[d] += scale * dp[j] * (double)q[d];
+            }
+        }
+    }
+}
+
+int oracle_attention_bwd(const float *Q, const float *K, const float *V, const float *dO,
+                         double *dQ, double *dK, double *dV,
+                         int64_t B, int64_t H, int64_t N, int64_t D,
+                         int causal, double scale, const int32_t *kv_len, int nthreads)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return -1;
+    if (B < 0 || H < 0 || N < 0 || D <= 0) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double *o = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!p || !dp || !o) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t head = 0; head < B * H; ++head) {
+            if (!p || !dp || !o) continue;
+            oracle_bwd_head(Q, K, V, dO, dQ, dK, dV, N, D, head, key_length(kv_len, head / H, N),
+                            causal, scale, p, dp, o);
+        }
+        free(p);
+        free(dp);
+        free(o);
+    }
+    return bad ? -1 : 0;
+}
