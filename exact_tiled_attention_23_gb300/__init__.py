@@ -23,6 +23,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "
            "fa_device_status", "fa_last_error_detail", "fa_fwd_splitkv",
            "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "FA_MAX_SPLITS",
            "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES", "fa_fwd_f16",
+           "fa_bwd", "fa_bwd_workspace_bytes", "backward",
            "forward", "build"]
 
 FA_OK = 0
@@ -87,6 +88,11 @@ def load():
         lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp,
                                                i32, vp]
         lib.fa_fwd_splitkv_noalloc.restype = i32
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
+                               ctypes.c_size_t, vp]
+        lib.fa_bwd.restype = i32
+        lib.fa_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         _lib = lib
         return lib
 
@@ -126,6 +132,17 @@ def fa_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, n
     share the scratch and race."""
     return int(load().fa_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, H, N, D, int(bool(causal)),
                                              float(scale), kv_len, int(num_splits), stream))
+
+
+def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, causal, scale, kv_len, workspace,
+           workspace_bytes, stream) -> int:
+    """bf16 backward by recomputation; pointers are device addresses or None."""
+    return int(load().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, int(bool(causal)),
+                             float(scale), kv_len, workspace, int(workspace_bytes), stream))
+
+
+def fa_bwd_workspace_bytes(B, H, N, D) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, D))
 
 
 def fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits) -> int:
@@ -217,3 +234,39 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
 
 def default_scale(D: int) -> float:
     return 1.0 / math.sqrt(D)
+
+
+def backward(q, k, v, o, do, lse, causal: bool = True, scale=None, kv_len=None, workspace=None,
+             stream=None):
+    """(dQ, dK, dV) of sum(O * dO) for O, LSE = forward(q, k, v, ...), bf16
+    CUDA tensors [B, H, N, D] (LSE fp32 [B, H, N]).  The workspace (a CUDA
+    tensor of at least fa_bwd_workspace_bytes bytes) is allocated here with
+    torch when not given."""
+    import torch
+
+    for x in (q, k, v, o, do):
+        if x.shape != q.shape or x.dtype != torch.bfloat16 or not x.is_cuda:
+            raise ValueError("q, k, v, o, do must be bf16 CUDA tensors of one shape [B, H, N, D]")
+    q, k, v, o, do = (x.contiguous() for x in (q, k, v, o, do))
+    B, H, N, D = q.shape
+    lse = lse.contiguous()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    need = fa_bwd_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    kv_ptr = None
+    if kv_len is not None:
+        if kv_len.dtype != torch.int32 or not kv_len.is_cuda or kv_len.numel() != B:
+            raise ValueError("kv_len must be an int32 CUDA tensor with B entries")
+        kv_len = kv_len.contiguous()
+        kv_ptr = kv_len.data_ptr()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, causal,
+                float("nan") if scale is None else float(scale), kv_ptr, workspace.data_ptr(),
+                workspace.numel() * workspace.element_size(), sp)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv

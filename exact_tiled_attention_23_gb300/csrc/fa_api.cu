@@ -250,6 +250,61 @@ fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, 
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int D)
+{
+    if (B < 0 || H < 0 || N < 0 || D <= 0) return 0;
+    return (size_t)B * (size_t)H * (size_t)N * ((size_t)D + 1) * sizeof(float);
+}
+
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                 const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                 int causal, float scale, const int32_t *kv_len, void *workspace,
+                 size_t workspace_bytes, void *stream)
+{
+    fa_status st = check_common(Q, K, V, dQ, B, H, N, D);
+    if (st != FA_OK) return st;
+    if ((int64_t)B * H * N == 0) return FA_OK;
+    if (!O || !dO || !LSE || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const void *ptrs16[] = {Q, K, V, O, dO, dQ, dK, dV, workspace};
+    for (const void *ptr : ptrs16)
+        if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(LSE) & 3u) || (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)))
+        return FA_ERR_INVALID_ARG;
+    if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, D)) return FA_ERR_INVALID_ARG;
+    const int64_t ctas = (int64_t)B * H * (((int64_t)N + 127) / 128);
+    if (ctas > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+    const int64_t BH = (int64_t)B * H;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_bf16_map(&tq, Q, BH, N, D) || !encode_bf16_map(&tk, K, BH, N, D) ||
+        !encode_bf16_map(&tv, V, BH, N, D) || !encode_bf16_map(&tdo, dO, BH, N, D))
+        return FA_ERR_CUDA;
+    fa::BwdParams p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.d_o = dO;
+    p.lse = LSE;
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.kv_len = kv_len;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.D = D;
+    p.causal = causal ? 1 : 0;
+    p.scale = resolve_scale(scale, D);
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.wait_limit_ns = wait_limit_ns();
+    p.dq_acc = static_cast<float *>(workspace);
+    p.delta = p.dq_acc + (size_t)BH * N * D;
+    cudaError_t e = fa::launch_bwd_bf16(p, tq, tk, tv, tdo, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 const char *fa_status_string(fa_status s)
 {
     switch (s) {
@@ -264,9 +319,11 @@ const char *fa_status_string(fa_status s)
 
 fa_status fa_device_status(void *stream)
 {
-    uint32_t v = 0;
-    if (fa::read_and_clear_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess)
+    uint32_t v = 0, vb = 0;
+    if (fa::read_and_clear_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess ||
+        fa::read_and_clear_status_bwd(&vb) != cudaSuccess)
         return FA_ERR_CUDA;
+    v |= vb;
     if (v) {
         g_last_detail = v;
         if (v & fa::kStatusTimeout) return FA_ERR_TIMEOUT;

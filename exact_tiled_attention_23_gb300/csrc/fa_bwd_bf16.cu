@@ -1,0 +1,441 @@
+// fa_bwd_bf16.cu -- bf16 attention backward on the Blackwell tensor cores.
+//
+// The backward by recomputation of "FlashAttention" (module F08, Math:
+// "backward pass via recomputation and the rowsum(dP*P) = rowsum(dO*O)
+// identity"; "vectorized-flash-attention-kernel", Key design decisions 4:
+// the forward's saved row statistics rebuild P without a second softmax).
+// With P = 2^(S*scale*log2e - LSE*log2e) rebuilt from the forward's LSE:
+//
+//   dV = P^T dO,   dP = dO V^T,   Delta = rowsum(dO * O),
+//   dS = P * (dP - Delta),   dQ = scale * dS K,   dK = scale * dS^T Q.
+//
+// Kernels, all on the caller's stream:
+//   1. bwd_prep_kernel: Delta per query row (fp32) and a zeroed fp32 dQ
+//      accumulator, both in the caller's workspace;
+//   2. bwd_kernel<D>: one CTA per (batch*head, 128-key tile).  K_j, V_j stay
+//      in shared memory; the query tiles that see them stream through a
+//      two-stage TMA ring with their dO.  Per query tile, in tensor memory
+//      (one TMEM lane per key):
+//        S^T = K_j Q_i^T and dP^T = V_j dO_i^T        (SS MMAs)
+//        P^T, dS^T (bf16) written back over them by the key-row threads
+//        dV += P^T dO_i and dK += dS^T Q_i             (TS MMAs, TMEM accumulators)
+//        dQ_i = dS K_j                                 (SS MMA, dS staged in shared memory)
+//      and the threads add dQ_i into the fp32 accumulator with vector
+//      atomics; at the end dK (times scale) and dV are written as bf16;
+//   3. bwd_dq_kernel: dQ = scale * accumulator, rounded to bf16.
+// Keys at or past kv_len get zero dK, dV; query rows whose mask hides every
+// key contribute nothing (P = 0 there).
+#include "fa_internal.h"
+#include "fa_tc_common.cuh"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+
+__device__ uint32_t g_status_bwd;
+
+namespace {
+
+constexpr int BK = 128;              // keys per CTA (= TMEM lanes of S^T, dP^T, dK, dV)
+constexpr int BQ = 128;              // query rows per step
+constexpr int kThreads = 256;        // warp 0 TMA, warp 1 MMA, warps 4-7 key/query rows
+constexpr int kWorkWarp0 = 4;
+
+template <int D>
+struct BwdLayout {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kChunkBytes = 128 * 128;             // one 128-row x 64-column bf16 box
+    static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x D
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kTileBytes;
+    static constexpr int kStages = 2;
+    static constexpr int kStageOff = 2 * kTileBytes;          // stage s: Q_i then dO_i
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kDSOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kDSBytes = 2 * kChunkBytes;          // dS: 128 keys x 128 queries bf16
+    static constexpr int kSmemBytes = kDSOff + kDSBytes + 1024;   // + alignment slack
+    static constexpr uint32_t kTmemCols = 512;
+    // TMEM: S^T [0,128) then P^T (bf16) over [0,64) and dQ_i over [0,D);
+    // dP^T [128,256) then dS^T (bf16) over [128,192); dV and dK after them.
+    static constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
+    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(kSmemBytes + 2048 <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+           const BwdParams p)
+{
+    using Lay = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t bars[12];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_word;
+    __shared__ float lse2_s[BQ];     // LSE of the current query tile, log2 units (+inf: no row)
+    __shared__ float delta_s[BQ];    // Delta of the current query tile
+    uint64_t *kv_full = &bars[0];
+    uint64_t *stage_full = &bars[1];   // [2]
+    uint64_t *stage_empty = &bars[3];  // [2]
+    uint64_t *s_full = &bars[5];
+    uint64_t *p_ready = &bars[6];
+    uint64_t *dq_full = &bars[7];
+    uint64_t *dq_free = &bars[8];
+    uint64_t *acc_full = &bars[9];
+    uint64_t *mma_drain = &bars[10];
+    const Abort ab{&abort_word, &g_status_bwd};
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t BH = p.B * p.H;
+    const int64_t N = p.N;
+    // heaviest causal tiles first: key tile j sees query tiles j..nq-1
+    const int64_t jt = (int64_t)blockIdx.x / BH;
+    const int64_t bh = (int64_t)blockIdx.x % BH;
+    const int64_t b = bh / p.H;
+    const int64_t k0 = jt * BK;
+    int64_t L = N;
+    if (p.kv_len) {
+        L = p.kv_len[b];
+        L = L < 0 ? 0 : (L > N ? N : L);
+    }
+    const int64_t nq = (N + BQ - 1) / BQ;
+    const int64_t i0 = p.causal ? jt : 0;
+    const int n_iter = (k0 < L) ? (int)(nq - i0) : 0;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&stage_full[s], 1);
+            ptx::mbar_init(&stage_empty[s], 1);
+        }
+        ptx::mbar_init(s_full, 1);
+        ptx::mbar_init(p_ready, 128);
+        ptx::mbar_init(dq_full, 1);
+        ptx::mbar_init(dq_free, 128);
+        ptx::mbar_init(acc_full, 1);
+        ptx::mbar_init(mma_drain, 1);
+        abort_word = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&tmem_slot, Lay::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0 && n_iter > 0) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::tma_prefetch_desc(&tm_do);
+            ptx::mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
+            for (int c = 0; c < Lay::kChunks; ++c) {
+                ptx::tma_load_3d(smem + Lay::kKOff + c * Lay::kChunkBytes, &tm_k, kv_full, c * 64,
+                                 (int32_t)k0, (int32_t)bh);
+                ptx::tma_load_3d(smem + Lay::kVOff + c * Lay::kChunkBytes, &tm_v, kv_full, c * 64,
+                                 (int32_t)k0, (int32_t)bh);
+            }
+            uint32_t issued = 0;
+            for (int it = 0; it < n_iter; ++it) {
+                const int s = it & 1;
+                if (it >= 2 &&
+                    !wait_bounded(&stage_empty[s], ((it >> 1) - 1) & 1, p.wait_limit_ns, kSiteSlotEmpty, ab))
+                    break;
+                const int32_t qrow = (int32_t)((i0 + it) * BQ);
+                uint8_t *st = smem + Lay::kStageOff + s * Lay::kStageBytes;
+                ptx::mbar_arrive_expect_tx(&stage_full[s], 2 * Lay::kTileBytes);
+                for (int c = 0; c < Lay::kChunks; ++c) {
+                    ptx::tma_load_3d(st + c * Lay::kChunkBytes, &tm_q, &stage_full[s], c * 64, qrow, (int32_t)bh);
+                    ptx::tma_load_3d(st + Lay::kTileBytes + c * Lay::kChunkBytes, &tm_do, &stage_full[s],
+                                     c * 64, qrow, (int32_t)bh);
+                }
+                issued = (uint32_t)it + 1;
+            }
+            // Drain: every copy has landed before the CTA exits.
+            wait_bounded(kv_full, 0, p.wait_limit_ns, kSiteDrain, ab, false);
+            for (uint32_t it = issued >= 2 ? issued - 2 : 0; it < issued; ++it)
+                wait_bounded(&stage_full[it & 1], (it >> 1) & 1, p.wait_limit_ns, kSiteDrain, ab, false);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0 && n_iter > 0) {
+            const uint32_t base = ptx::smem_u32(smem);
+            // K-major operands (rows of 128-byte swizzled chunks)
+            const uint64_t dK_km = make_sdesc(base + Lay::kKOff, 16, 1024);
+            const uint64_t dV_km = make_sdesc(base + Lay::kVOff, 16, 1024);
+            // MN-major operands: 8 rows of 128 B per 1024 B group, 64-column
+            // chunks one box (16 KiB) apart; a K-step of 16 rows is 2 KiB
+            const uint64_t dK_mn = make_sdesc(base + Lay::kKOff, Lay::kChunkBytes, 1024);
+            const uint64_t dS_mn = make_sdesc(base + Lay::kDSOff, Lay::kChunkBytes, 1024);
+            constexpr uint32_t id_st = make_idesc(BK, BQ, 0, 0);    // S^T, dP^T: 128 keys x 128 queries
+            constexpr uint32_t id_acc = make_idesc(BK, D, 0, 1);    // dV, dK: A in TMEM, B MN-major
+            constexpr uint32_t id_dq = make_idesc(BQ, D, 1, 1);     // dQ: A = dS MN-major, B = K MN-major
+
+            bool ok = wait_bounded(kv_full, 0, p.wait_limit_ns, kSiteQFull, ab);
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int s = it & 1;
+                const uint32_t st = base + Lay::kStageOff + s * Lay::kStageBytes;
+                const uint64_t dQ_km = make_sdesc(st, 16, 1024);
+                const uint64_t dO_km = make_sdesc(st + Lay::kTileBytes, 16, 1024);
+                const uint64_t dQ_mn = make_sdesc(st, Lay::kChunkBytes, 1024);
+                const uint64_t dO_mn = make_sdesc(st + Lay::kTileBytes, Lay::kChunkBytes, 1024);
+                if (!wait_bounded(&stage_full[s], (it >> 1) & 1, p.wait_limit_ns, kSiteSlotFull, ab)) break;
+                if (it > 0 && !wait_bounded(dq_free, (it - 1) & 1, p.wait_limit_ns, kSitePFull, ab)) break;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t off = (uint64_t)(((k / 4) * Lay::kChunkBytes + (k % 4) * 32) >> 4);
+                    ptx::mma_ss(tmem + Lay::kColST, dK_km + off, dQ_km + off, id_st, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t off = (uint64_t)(((k / 4) * Lay::kChunkBytes + (k % 4) * 32) >> 4);
+                    ptx::mma_ss(tmem + Lay::kColDPT, dV_km + off, dO_km + off, id_st, k > 0);
+                }
+                ptx::mma_commit(s_full);
+                if (!wait_bounded(p_ready, it & 1, p.wait_limit_ns, kSitePFull, ab)) break;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < BQ / 16; ++k) {
+                    const uint64_t off = (uint64_t)((k * 2048) >> 4);
+                    ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColST + k * 8, dO_mn + off, id_acc,
+                                (it > 0 || k > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < BQ / 16; ++k) {
+                    const uint64_t off = (uint64_t)((k * 2048) >> 4);
+                    ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDPT + k * 8, dQ_mn + off, id_acc,
+                                (it > 0 || k > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t off = (uint64_t)((k * 2048) >> 4);
+                    ptx::mma_ss(tmem + Lay::kColST, dS_mn + off, dK_mn + off, id_dq, k > 0);
+                }
+                ptx::mma_commit(dq_full);
+                ptx::mma_commit(&stage_empty[s]);
+                if (it + 1 == n_iter) ptx::mma_commit(acc_full);
+            }
+            ptx::mma_commit(mma_drain);
+            wait_bounded(mma_drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
+        }
+    } else if (warp >= kWorkWarp0) {
+        // ================= key rows: P^T, dS^T; query rows: dQ =================
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;                      // TMEM lane: key t (and query t for dQ)
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int64_t key = k0 + t;
+        const bool key_ok = key < L;
+        const float sl2 = p.scale_log2;
+        const uint32_t ds_base = ptx::smem_u32(smem + Lay::kDSOff);
+        bool ok = true;
+        for (int it = 0; it < n_iter && ok; ++it) {
+            const int64_t q0 = (i0 + it) * BQ;
+            // this query tile's LSE (log2 units) and Delta, shared by all key rows
+            ptx::bar_sync(1, 128);
+            {
+                const int64_t qr = q0 + t;
+                lse2_s[t] = qr < N ? p.lse[bh * N + qr] * 1.4426950408889634f : INFINITY;
+                delta_s[t] = qr < N ? p.delta[bh * N + qr] : 0.f;
+            }
+            ptx::bar_sync(1, 128);
+            // all 128 threads agree on going on, so the named barriers stay matched
+            ok = ptx::bar_and(1, 128, wait_bounded(s_full, it & 1, p.wait_limit_ns, kSiteSFull, ab));
+            if (!ok) break;
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < BQ / 32; ++c) {
+                uint32_t sv[32], dpv[32];
+                ptx::tmem_ld32(tmem + lane_off + Lay::kColST + c * 32, sv);
+                ptx::tmem_ld32(tmem + lane_off + Lay::kColDPT + c * 32, dpv);
+                ptx::tmem_wait_ld();
+                uint32_t pw[16], dsw[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int64_t qa = q0 + c * 32 + e;
+                    const bool va = key_ok && (!p.causal || qa >= key);
+                    const bool vb = key_ok && (!p.causal || qa + 1 >= key);
+                    const float pa = va ? ptx::ex2_approx(fmaf(u2f(sv[e]), sl2, -lse2_s[c * 32 + e])) : 0.f;
+                    const float pb = vb ? ptx::ex2_approx(fmaf(u2f(sv[e + 1]), sl2, -lse2_s[c * 32 + e + 1])) : 0.f;
+                    const float da = pa * (u2f(dpv[e]) - delta_s[c * 32 + e]);
+                    const float db = pb * (u2f(dpv[e + 1]) - delta_s[c * 32 + e + 1]);
+                    pw[e / 2] = ptx::pack_bf16x2(pa, pb);
+                    dsw[e / 2] = ptx::pack_bf16x2(da, db);
+                }
+                ptx::tmem_st16(tmem + lane_off + Lay::kColST + c * 16, pw);
+                ptx::tmem_st16(tmem + lane_off + Lay::kColDPT + c * 16, dsw);
+                // dS row of key t into the MN-major, 128-byte-swizzled A operand
+                // of dQ = dS K: query chunk c*32.. = 4 units of 8 queries
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int qq = c * 32 + w * 8;            // first query of the unit
+                    const uint32_t unit = (uint32_t)((qq % 64) / 8) ^ (uint32_t)(t & 7);
+                    const uint32_t addr = ds_base + (uint32_t)(qq / 64) * Lay::kChunkBytes + (uint32_t)t * 128u + (unit << 4);
+                    ptx::st_shared_v4(addr, dsw[4 * w], dsw[4 * w + 1], dsw[4 * w + 2], dsw[4 * w + 3]);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(p_ready);
+
+            // dQ_i rows (TMEM lane t = query q0 + t) into the fp32 accumulator
+            ok = ptx::bar_and(1, 128, wait_bounded(dq_full, it & 1, p.wait_limit_ns, kSiteOFinal, ab));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int64_t qr = q0 + t;
+            float *acc = p.dq_acc + (bh * N + qr) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + lane_off + Lay::kColST + c * 32, v);
+                ptx::tmem_wait_ld();
+                if (qr < N) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        ptx::red_add_v4(acc + c * 32 + e, u2f(v[e]), u2f(v[e + 1]), u2f(v[e + 2]), u2f(v[e + 3]));
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(dq_free);
+        }
+
+        // ---- dK (times scale) and dV of this key tile ------------------------
+        bool have = ok && n_iter > 0;
+        if (n_iter > 0)
+            have = ptx::bar_and(1, 128, have && wait_bounded(acc_full, 0, p.wait_limit_ns, kSiteOFinal, ab));
+        if (have || n_iter == 0) {
+            ptx::tc_fence_after();
+            uint16_t *dk_row = static_cast<uint16_t *>(p.dk) + (bh * N + key) * D;
+            uint16_t *dv_row = static_cast<uint16_t *>(p.dv) + (bh * N + key) * D;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which ? Lay::kColDK : Lay::kColDV;
+                const float mul = which ? p.scale : 1.f;
+                uint16_t *dst_row = which ? dk_row : dv_row;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (n_iter > 0) {
+                        ptx::tmem_ld32(tmem + lane_off + col + c * 32, v);
+                        ptx::tmem_wait_ld();
+                    }
+                    if (key < N) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = n_iter > 0 ? ptx::pack_bf16x2(u2f(v[2 * e]) * mul, u2f(v[2 * e + 1]) * mul) : 0u;
+                        uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
+// Delta = rowsum(dO * O) per query row, and the zeroed fp32 dQ accumulator.
+// One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ d_o,
+                float *__restrict__ delta, float *__restrict__ dq_acc, int64_t rows)
+{
+    constexpr int kPer = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) {
+        const int64_t idx = row * D + lane * kPer + c;
+        s = fmaf(__uint_as_float((uint32_t)o[idx] << 16), __uint_as_float((uint32_t)d_o[idx] << 16), s);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) delta[row] = s;
+    float *acc = dq_acc + row * D + lane * kPer;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+}
+
+// dQ = scale * accumulator, rounded to bf16 (two elements per thread).
+__global__ void __launch_bounds__(256)
+bwd_dq_kernel(const float *__restrict__ dq_acc, uint16_t *__restrict__ dq, float scale, int64_t n2)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n2) return;
+    const float2 v = reinterpret_cast<const float2 *>(dq_acc)[i];
+    reinterpret_cast<uint32_t *>(dq)[i] = ptx::pack_bf16x2(v.x * scale, v.y * scale);
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t stream)
+{
+    using Lay = BwdLayout<D>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Lay::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int64_t rows = p.B * p.H * p.N;
+    bwd_prep_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(p.o), static_cast<const uint16_t *>(p.d_o), p.delta, p.dq_acc, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = p.B * p.H * ((p.N + BK - 1) / BK);
+    bwd_kernel<D><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t n2 = rows * D / 2;
+    bwd_dq_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t *>(p.dq),
+                                                                  p.scale, n2);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(const BwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                            const CUtensorMap &tm_v, const CUtensorMap &tm_do, cudaStream_t stream)
+{
+    if (p.D == 64) return launch_bwd_d<64>(p, tm_q, tm_k, tm_v, tm_do, stream);
+    if (p.D == 128) return launch_bwd_d<128>(p, tm_q, tm_k, tm_v, tm_do, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_status_bwd(uint32_t *out)
+{
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_bwd, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_status_bwd, &zero, sizeof(zero));
+        if (e != cudaSuccess) return e;
+    }
+    *out = v;
+    return cudaSuccess;
+}
+
+}  // namespace fa

@@ -34,6 +34,7 @@
 // the library's device status word, raises a CTA-wide abort flag, and every
 // role then drains its in-flight copies / MMAs, frees tensor memory and exits.
 #include "fa_internal.h"
+#include "fa_tc_common.cuh"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
@@ -76,60 +77,6 @@ struct Layout {
     static_assert((1 + 2 * kSlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
-// tcgen05 instruction descriptor, kind::f16: A and B both bf16 (or both
-// f16), fp32 accumulator.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int a_mn_major, int b_mn_major,
-                                                  bool f16 = false)
-{
-    return (1u << 4)                      // accumulator format: f32
-         | ((f16 ? 0u : 1u) << 7)         // A format: f16 = 0, bf16 = 1
-         | ((f16 ? 0u : 1u) << 10)        // B format: same as A
-         | ((uint32_t)a_mn_major << 15)
-         | ((uint32_t)b_mn_major << 16)
-         | ((uint32_t)(N >> 3) << 17)
-         | ((uint32_t)(M >> 4) << 24);
-}
-
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand.
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;               // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;               // swizzle: 128 B
-    return d;
-}
-
-struct Abort {
-    volatile int *flag;
-};
-
-// Bounded wait on phase `parity` of `bar`.  Returns false when the budget ran
-// out (the status word records `site`) or, if `follow_abort`, as soon as
-// another thread of the CTA has aborted.
-__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
-                                             uint32_t site, Abort ab, bool follow_abort = true)
-{
-    if (ptx::mbar_test(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer_ns();
-    uint32_t spins = 0;
-    while (true) {
-        if (ptx::mbar_test(bar, parity)) return true;
-        if ((++spins & 63u) == 0) {
-            if (follow_abort && *ab.flag) return false;
-            if (ptx::globaltimer_ns() - t0 > limit_ns) {
-                atomicOr(&g_status, kStatusTimeout | (site << 8));
-                *ab.flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
 template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -150,7 +97,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t *mma_drain = o_final + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
-    const Abort ab{abort_word};
+    const Abort ab{abort_word, &g_status};
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;

@@ -48,6 +48,21 @@ struct FwdParams {
     float *part_lse;
 };
 
+// Arguments of the backward pass (bf16 tensors, fp32 LSE and workspace).
+struct BwdParams {
+    const void *q, *k, *v, *o, *d_o;
+    const float *lse;
+    void *dq, *dk, *dv;
+    const int32_t *kv_len;    // may be null (= N)
+    int64_t B, H, N, D;
+    int causal;
+    float scale;
+    float scale_log2;
+    uint64_t wait_limit_ns;
+    float *delta;             // workspace: rowsum(dO * O), [B*H*N]
+    float *dq_acc;            // workspace: fp32 dQ accumulator, [B*H*N*D]
+};
+
 // Launchers (return the CUDA error of the launch).
 cudaError_t launch_fwd_fp32(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
@@ -57,7 +72,13 @@ cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const C
 cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                   const CUtensorMap &tm_v, cudaStream_t stream);
 
+// Backward: Delta / accumulator preparation, the tensor-core kernel, dQ.
+cudaError_t launch_bwd_bf16(const BwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                            const CUtensorMap &tm_v, const CUtensorMap &tm_do, cudaStream_t stream);
+
 // Read-and-clear of the device status word (synchronises `stream` first).
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out);
+// The backward kernels' status word (call after read_and_clear_status).
+cudaError_t read_and_clear_status_bwd(uint32_t *out);
 
 }  // namespace fa

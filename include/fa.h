@@ -174,6 +174,40 @@ fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, vo
                                  int B, int H, int N, int D, int causal, float scale,
                                  const int32_t *kv_len, int num_splits, void *stream);
 
+/*
+ * fa_bwd -- backward pass of fa_fwd by recomputation ("FlashAttention"
+ * module F08, Math: backward via recomputation and the identity
+ * rowsum(dP*P) = rowsum(dO*O); "vectorized-flash-attention-kernel", Key
+ * design decisions 4: the saved row statistics rebuild P).  Computes the
+ * gradients of sum(O * dO) for O = fa_fwd(Q, K, V, ...):
+ *
+ *     P = exp(scale*Q K^T + mask - LSE),  dV = P^T dO,  dP = dO V^T,
+ *     Delta = rowsum(dO * O),  dS = P * (dP - Delta),
+ *     dQ = scale * dS K,  dK = scale * dS^T Q.
+ *
+ *   Q, K, V, O, dO  const bf16 [B,H,N,D]: the forward's inputs and output
+ *                   and the upstream gradient; 16-byte aligned.
+ *   LSE             const float [B,H,N]: the LSE fa_fwd returned.
+ *   dQ, dK, dV      bf16 [B,H,N,D] outputs (fp32 accumulation, rounded to
+ *                   nearest even); keys at or past kv_len get zero dK, dV.
+ *   B,H,N,D, causal, scale, kv_len: as in the forward call; D in {64, 128}.
+ *   workspace       caller-owned device memory, 16-byte aligned, of at least
+ *                   fa_bwd_workspace_bytes(B,H,N,D) bytes (an fp32 dQ
+ *                   accumulator and Delta); fully rewritten by each call;
+ *                   calls that may overlap need separate workspaces.
+ * dQ is summed across key tiles with fp32 atomic adds, so its last bits may
+ * differ from run to run; dK and dV are deterministic.  Four kernels are
+ * enqueued on `stream`.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a
+ * missing or too small workspace.
+ */
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                 const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                 int causal, float scale, const int32_t *kv_len, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace fa_bwd needs: B*H*N*(D + 1)*4 (0 for invalid sizes). */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int D);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *fa_status_string(fa_status s);
 

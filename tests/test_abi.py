@@ -114,3 +114,16 @@ def test_splitkv_argument_checks(lib):
     assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, 2, P, need - 1, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 96, 1, NAN, None, 2, P, big, None) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fwd_splitkv(None, None, None, None, None, 1, 1, 0, 64, 1, NAN, None, 2, None, 0, None) == fa.FA_OK
+
+
+def test_bwd_workspace_and_argument_checks(lib):
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 100 * 65 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, -1, 64) == 0
+    big = 1 << 40
+    assert fa.fa_bwd(P, P, P, P, P, P, P, P, P, 1, 1, 16, 96, 1, NAN, None, P, big, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd(P, P, P, None, P, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, P, big, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd(P, P, P, P, P, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, None, big, None) == fa.FA_ERR_INVALID_ARG
+    need = fa.fa_bwd_workspace_bytes(1, 1, 16, 64)
+    assert fa.fa_bwd(P, P, P, P, P, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, P, need - 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd(P, P, P, P, P + 8, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, P, big, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd(None, None, None, None, None, None, None, None, None, 1, 1, 0, 64, 1, NAN, None, None, 0, None) == fa.FA_OK

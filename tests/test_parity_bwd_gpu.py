@@ -1,0 +1,77 @@
+"""Parity of the bf16 backward (fa_bwd) with the fp64 backward oracle.
+
+Tolerance (bf16 inputs and outputs, fp32 accumulation; derived in the
+design notes): for each of dQ, dK, dV, the largest error is at most 2e-2 of
+the tensor's largest reference entry and the mean error at most 1e-2 of its
+mean reference magnitude.  P and dS are rounded to bf16 for the tensor-core
+products (relative 2^-9 each), O is the forward's bf16 output, and the
+gradients are rounded once more to bf16 on output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_23_gb300 as fa
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+MAX_REL, MEAN_REL = 2e-2, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    fa.build()
+    fa.load()
+    oracle.library()
+
+
+def run_case(B, H, N, D, causal, kv_len, seed):
+    inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=causal, seed=seed, kv_len=kv_len)
+    g = torch.Generator("cpu").manual_seed(seed + 77)
+    do = torch.randn((B, H, N, D), generator=g).to(torch.bfloat16)
+    q, k, v, dog = inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), do.cuda()
+    kv = inp.kv_len.cuda() if inp.kv_len is not None else None
+    o, lse = fa.forward(q, k, v, causal=causal, kv_len=kv)
+    dq, dk, dv = fa.backward(q, k, v, o, dog, lse, causal=causal, kv_len=kv)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    ref = oracle.attention_bwd(inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(),
+                               do.float().numpy(), causal=causal,
+                               kv_len=None if inp.kv_len is None else inp.kv_len.numpy())
+    stats = {}
+    for name, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        gn = got.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(gn)), name
+        err = np.abs(gn - r)
+        scale_max = np.abs(r).max()
+        scale_mean = np.abs(r).mean()
+        stats[name] = (err.max() / max(scale_max, 1e-30), err.mean() / max(scale_mean, 1e-30))
+        if scale_max == 0:
+            assert np.all(gn == 0), name
+            continue
+        assert err.max() <= MAX_REL * scale_max, (name, stats[name])
+        assert err.mean() <= MEAN_REL * scale_mean, (name, stats[name])
+    if inp.kv_len is not None:
+        for bi in range(B):
+            L = int(inp.kv_len[bi])
+            assert bool((dk[bi, :, L:] == 0).all()) and bool((dv[bi, :, L:] == 0).all())
+    return stats
+
+
+CASES = [
+    # B, H, N, D, causal, kv_len
+    (1, 1, 128, 64, True, None),
+    (1, 2, 256, 128, False, None),
+    (2, 2, 300, 64, True, [300, 0]),
+    (1, 2, 640, 128, True, [500]),
+    (2, 1, 777, 128, False, [777, 129]),
+    (1, 2, 1024, 64, True, None),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len", CASES)
+def test_bwd_matches_oracle(B, H, N, D, causal, kv_len):
+    stats = run_case(B, H, N, D, causal, kv_len, seed=N + D)
+    print(stats)
