@@ -276,8 +276,24 @@ def run_ours(args, rank, world, local):
         ws_bytes = fa.fa_fwd_splitkv_workspace_bytes(B, H, N, D, splits)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)   # outside the timed region
 
+    if args.pass_ == "bwd":
+        if w.dtype != "bf16":
+            raise SystemExit("--pass bwd needs a bf16 workload")
+        # the forward's outputs and an upstream gradient, made outside the timed region
+        fa.forward(q, k, v, causal=w.causal, kv_len=kv, out=o, lse=lse)
+        gen = torch.Generator("cpu").manual_seed(w.seed + 99)
+        d_o = torch.randn(q.shape, generator=gen).to(torch.bfloat16).to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        bwd_ws_bytes = fa.fa_bwd_workspace_bytes(B, H, N, D)
+        bwd_ws = torch.empty(bwd_ws_bytes, dtype=torch.uint8, device=dev)
+        flops = 10.0 * D * pairs          # five products of 2*D flops per visible pair
+
     def step():
-        if splits is not None:
+        if args.pass_ == "bwd":
+            st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(),
+                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
+                           w.causal, float("nan"), kv_ptr, bwd_ws.data_ptr(), bwd_ws_bytes, sp)
+        elif splits is not None:
             st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                    B, H, N, D, w.causal, float("nan"), kv_ptr, splits,
                                    workspace.data_ptr(), ws_bytes, sp)
@@ -334,7 +350,8 @@ def run_ours(args, rank, world, local):
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                    "peak_kind": f"{peak_kind} dense bf16 (burst)", "kernel": "fwd_bf16_kernel",
+                    "peak_kind": f"{peak_kind} dense bf16 (burst)",
+                    "kernel": "bwd_kernel" if args.pass_ == "bwd" else "fwd_bf16_kernel",
                     "flops_per_launch": flops}
     else:
         # fp32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 flops x max SM clock
@@ -350,7 +367,7 @@ def run_ours(args, rank, world, local):
 
     # ---- e2e through the C ABI with host buffers ---------------------------
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.pass_ == "fwd":
         hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
@@ -394,7 +411,8 @@ def run_ours(args, rank, world, local):
                "sample": f"{n} random query rows of {w.name} ({dt:.1f} s), fp64 two-pass naive attention"}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if args.pass_ == "fwd" else METRIC.replace("attention fwd", "attention bwd"),
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "causal": w.causal,
@@ -402,12 +420,13 @@ def run_ours(args, rank, world, local):
                    "l2": ("256 MiB write before every step (flush not timed)" if flush else
                           "inputs (Q,K,V) larger than L2; no flush between steps"),
                    "parallelism": f"replicas x{world} (no exchange)",
-                   "path": "fa_fwd" if splits is None else f"fa_fwd_splitkv (splits={splits})"},
+                   "path": ("fa_bwd" if args.pass_ == "bwd" else
+                            "fa_fwd" if splits is None else f"fa_fwd_splitkv (splits={splits})")},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 if splits is not None else 1),
+        "gpu_launches": args.steps * (3 if args.pass_ == "bwd" else 2 if splits is not None else 1),
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -434,6 +453,8 @@ def main():
                     help="override the element type of a 16-bit workload")
     ap.add_argument("--splits", type=int, default=None,
                     help="time the split-KV path with this many key ranges (0 = automatic)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward pass (fa_bwd)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
