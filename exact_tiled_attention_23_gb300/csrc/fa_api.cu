@@ -111,6 +111,22 @@ bool encode_map16(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int64
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over the fp32 dQ accumulator [B*H, N, D]: box = 32 columns (128 B)
+// x 128 rows, 128-byte swizzle; rows past N are clipped by reduce-adds.
+bool encode_dq_acc_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int64_t D)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)N * D * 4};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_bf16_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int64_t D)
 {
     return encode_map16(m, base, BH, N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
@@ -276,9 +292,10 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     if (ctas > INT32_MAX) return FA_ERR_INVALID_ARG;
 
     const int64_t BH = (int64_t)B * H;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!encode_bf16_map(&tq, Q, BH, N, D) || !encode_bf16_map(&tk, K, BH, N, D) ||
-        !encode_bf16_map(&tv, V, BH, N, D) || !encode_bf16_map(&tdo, dO, BH, N, D))
+        !encode_bf16_map(&tv, V, BH, N, D) || !encode_bf16_map(&tdo, dO, BH, N, D) ||
+        !encode_dq_acc_map(&tdq, workspace, BH, N, D))
         return FA_ERR_CUDA;
     fa::BwdParams p{};
     p.q = Q;
@@ -301,7 +318,7 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     p.wait_limit_ns = wait_limit_ns();
     p.dq_acc = static_cast<float *>(workspace);
     p.delta = p.dq_acc + (size_t)BH * N * D;
-    cudaError_t e = fa::launch_bwd_bf16(p, tq, tk, tv, tdo, static_cast<cudaStream_t>(stream));
+    cudaError_t e = fa::launch_bwd_bf16(p, tq, tk, tv, tdo, tdq, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

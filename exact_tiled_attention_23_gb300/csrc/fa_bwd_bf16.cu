@@ -20,8 +20,9 @@
 //        P^T, dS^T (bf16) written back over them by the key-row threads
 //        dV += P^T dO_i and dK += dS^T Q_i             (TS MMAs, TMEM accumulators)
 //        dQ_i = dS K_j                                 (SS MMA, dS staged in shared memory)
-//      and the threads add dQ_i into the fp32 accumulator with vector
-//      atomics; at the end dK (times scale) and dV are written as bf16;
+//      and dQ_i is added into the fp32 accumulator by TMA reduce-add of
+//      staged 32-column boxes; at the end dK (times scale) and dV are
+//      written as bf16;
 //   3. bwd_dq_kernel: dQ = scale * accumulator, rounded to bf16.
 // Keys at or past kv_len get zero dK, dV; query rows whose mask hides every
 // key contribute nothing (P = 0 there).
@@ -67,7 +68,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-           const BwdParams p)
+           const __grid_constant__ CUtensorMap tm_dq, const BwdParams p)
 {
     using Lay = BwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -76,8 +77,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     __shared__ uint64_t bars[12];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_word;
-    __shared__ float lse2_s[BQ];     // LSE of the current query tile, log2 units (+inf: no row)
-    __shared__ float delta_s[BQ];    // Delta of the current query tile
+    __shared__ __align__(16) float lse2_s[BQ];     // LSE of the current query tile, log2 units (+inf: no row)
+    __shared__ __align__(16) float delta_s[BQ];    // Delta of the current query tile
     uint64_t *kv_full = &bars[0];
     uint64_t *stage_full = &bars[1];   // [2]
     uint64_t *stage_empty = &bars[3];  // [2]
@@ -259,16 +260,30 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 ptx::tmem_ld32(tmem + lane_off + Lay::kColST + c * 32, sv);
                 ptx::tmem_ld32(tmem + lane_off + Lay::kColDPT + c * 32, dpv);
                 ptx::tmem_wait_ld();
+                // this chunk's 32 LSE / Delta values (broadcast smem reads) and the
+                // first visible query: causal hides q < key, padding hides the row
+                float lse_c[32], dl_c[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(&lse2_s[c * 32 + e]);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(&delta_s[c * 32 + e]);
+                    lse_c[e] = a4.x; lse_c[e + 1] = a4.y; lse_c[e + 2] = a4.z; lse_c[e + 3] = a4.w;
+                    dl_c[e] = d4.x; dl_c[e + 1] = d4.y; dl_c[e + 2] = d4.z; dl_c[e + 3] = d4.w;
+                }
+                int e_min = 0;
+                if (!key_ok) {
+                    e_min = 32;
+                } else if (p.causal) {
+                    const int64_t d0 = key - (q0 + c * 32);
+                    e_min = d0 <= 0 ? 0 : (d0 >= 32 ? 32 : (int)d0);
+                }
                 uint32_t pw[16], dsw[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const int64_t qa = q0 + c * 32 + e;
-                    const bool va = key_ok && (!p.causal || qa >= key);
-                    const bool vb = key_ok && (!p.causal || qa + 1 >= key);
-                    const float pa = va ? ptx::ex2_approx(fmaf(u2f(sv[e]), sl2, -lse2_s[c * 32 + e])) : 0.f;
-                    const float pb = vb ? ptx::ex2_approx(fmaf(u2f(sv[e + 1]), sl2, -lse2_s[c * 32 + e + 1])) : 0.f;
-                    const float da = pa * (u2f(dpv[e]) - delta_s[c * 32 + e]);
-                    const float db = pb * (u2f(dpv[e + 1]) - delta_s[c * 32 + e + 1]);
+                    const float pa = e >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[e]), sl2, -lse_c[e])) : 0.f;
+                    const float pb = e + 1 >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[e + 1]), sl2, -lse_c[e + 1])) : 0.f;
+                    const float da = pa * (u2f(dpv[e]) - dl_c[e]);
+                    const float db = pb * (u2f(dpv[e + 1]) - dl_c[e + 1]);
                     pw[e / 2] = ptx::pack_bf16x2(pa, pb);
                     dsw[e / 2] = ptx::pack_bf16x2(da, db);
                 }
@@ -293,22 +308,47 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             ok = ptx::bar_and(1, 128, wait_bounded(dq_full, it & 1, p.wait_limit_ns, kSiteOFinal, ab));
             if (!ok) break;
             ptx::tc_fence_after();
-            const int64_t qr = q0 + t;
-            float *acc = p.dq_acc + (bh * N + qr) * D;
+            // Each 32-column chunk of dQ_i (row t = query q0 + t) is staged in the
+            // dS buffer (free: dQ = dS K has read it) as a 128-row x 128-byte box
+            // with the 16-byte units of row r XOR-swizzled by (r & 7) -- the
+            // shared-memory form of a 128-byte-swizzled TMA box -- and one thread
+            // hands it to the TMA engine, which adds it into the fp32 accumulator
+            // (rows at or past N are clipped by the tensor map).
+            float *stage = reinterpret_cast<float *>(smem + Lay::kDSOff);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
+                float *buf = stage + (c & 1) * (BQ * 32);
+                if (c >= 2) {
+                    // the reduce that read this buffer two chunks ago is done
+                    if (t == 0) ptx::bulk_wait_group_read<1>();
+                    ptx::bar_sync(1, 128);
+                }
                 uint32_t v[32];
                 ptx::tmem_ld32(tmem + lane_off + Lay::kColST + c * 32, v);
                 ptx::tmem_wait_ld();
-                if (qr < N) {
+                if (c + 1 == D / 32) {
+                    // all of dQ_i is in registers or staged: TMEM may take the next S^T
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(dq_free);
+                }
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        ptx::red_add_v4(acc + c * 32 + e, u2f(v[e]), u2f(v[e + 1]), u2f(v[e + 2]), u2f(v[e + 3]));
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<uint4 *>(buf + t * 32 + ((e ^ (t & 7)) << 2)) =
+                        make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                ptx::fence_proxy_async_smem();
+                ptx::bar_sync(1, 128);
+                if (t == 0) {
+                    ptx::tma_reduce_add_3d(&tm_dq, buf, c * 32, (int32_t)q0, (int32_t)bh);
+                    ptx::bulk_commit_group();
                 }
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(dq_free);
+            // the staging area is the next tile's dS buffer
+            if (t == 0) ptx::bulk_wait_group_read<0>();
+            ptx::bar_sync(1, 128);
         }
+
+        // every reduce-add this thread issued has reached global memory
+        if (t == 0) ptx::bulk_wait_group_all();
 
         // ---- dK (times scale) and dV of this key tile ------------------------
         bool have = ok && n_iter > 0;
@@ -389,7 +429,8 @@ bwd_dq_kernel(const float *__restrict__ dq_acc, uint16_t *__restrict__ dq, float
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                         const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t stream)
+                         const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
+                         cudaStream_t stream)
 {
     using Lay = BwdLayout<D>;
     static bool configured = false;
@@ -405,7 +446,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t ctas = p.B * p.H * ((p.N + BK - 1) / BK);
-    bwd_kernel<D><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    bwd_kernel<D><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t n2 = rows * D / 2;
@@ -417,10 +458,11 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
 }  // namespace
 
 cudaError_t launch_bwd_bf16(const BwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                            const CUtensorMap &tm_v, const CUtensorMap &tm_do, cudaStream_t stream)
+                            const CUtensorMap &tm_v, const CUtensorMap &tm_do, const CUtensorMap &tm_dq,
+                            cudaStream_t stream)
 {
-    if (p.D == 64) return launch_bwd_d<64>(p, tm_q, tm_k, tm_v, tm_do, stream);
-    if (p.D == 128) return launch_bwd_d<128>(p, tm_q, tm_k, tm_v, tm_do, stream);
+    if (p.D == 64) return launch_bwd_d<64>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
+    if (p.D == 128) return launch_bwd_d<128>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
     return cudaErrorInvalidValue;
 }
 

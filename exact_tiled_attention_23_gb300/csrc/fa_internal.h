@@ -74,7 +74,8 @@ cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, c
 
 // Backward: Delta / accumulator preparation, the tensor-core kernel, dQ.
 cudaError_t launch_bwd_bf16(const BwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                            const CUtensorMap &tm_v, const CUtensorMap &tm_do, cudaStream_t stream);
+                            const CUtensorMap &tm_v, const CUtensorMap &tm_do, const CUtensorMap &tm_dq,
+                            cudaStream_t stream);
 
 // Read-and-clear of the device status word (synchronises `stream` first).
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out);

@@ -355,3 +355,45 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool pre
 
 }  // namespace ptx
 }  // namespace fa
+
+namespace fa {
+namespace ptx {
+
+// 3-D tiled reduce-add of one shared-memory box into global memory (fp32
+// adds done by the TMA engine); completion is tracked with bulk groups.
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, const void *src, int32_t x,
+                                                  int32_t y, int32_t z)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N committed bulk groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+}  // namespace ptx
+}  // namespace fa
+
+namespace fa {
+namespace ptx {
+
+// Wait until every committed bulk group of this thread has completed (its
+// global writes included).
+__device__ __forceinline__ void bulk_wait_group_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+}  // namespace ptx
+}  // namespace fa
