@@ -50,6 +50,7 @@ METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak"
 L2_BYTES = 126 << 20
 UNIT = "TFLOP/s"
 FALLBACK_PEAK_TFLOPS = 1900.0   # used only when MEASURED_PEAKS.json is absent
+HOST_LEAD_CYCLES = 400_000      # about 0.2 ms of SM clock: the host's lead on the device
 
 
 def dist_env():
@@ -67,27 +68,35 @@ def measured_peaks():
     return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources each timed kernel is built from; a DRAM-traffic figure taken
+# by ncu stays valid only while these files are unchanged.
+KERNEL_SOURCES = {
+    "fwd_bf16_kernel": ("fa_fwd_bf16.cu", "fa_tc_common.cuh", "sm103_ptx.cuh", "fa_internal.h", "fa_api.cu"),
+    "bwd_kernel": ("fa_bwd_bf16.cu", "fa_tc_common.cuh", "sm103_ptx.cuh", "fa_internal.h", "fa_api.cu"),
+    "fwd_fp32_kernel": ("fa_fwd_fp32.cu", "fa_internal.h", "fa_api.cu"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_23_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+def profiled_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the kernel's current sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
     ent = rec.get(workload)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel") != kernel or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -323,10 +332,16 @@ def run_ours(args, rank, world, local):
         with torch.cuda.stream(stream):
             t_begin = torch.cuda.Event(enable_timing=True)
             t_end = torch.cuda.Event(enable_timing=True)
+            # A bounded device-side wait ahead of the loop (and after every
+            # flush) lets the host queue the next step before the GPU reaches
+            # it, so a step interval holds device time only, not the host's
+            # call overhead.  Neither wait lies inside a timed interval.
+            torch.cuda._sleep(HOST_LEAD_CYCLES * 4)
             t_begin.record(stream)
             for s in range(args.steps):
                 if flush:
                     scratch.fill_(s & 0xFF)     # evict the inputs from L2 (not timed)
+                    torch.cuda._sleep(HOST_LEAD_CYCLES)
                 starts[s].record(stream)
                 step()
                 ends[s].record(stream)
@@ -348,16 +363,16 @@ def run_ours(args, rank, world, local):
     if w.dtype in ("bf16", "fp16"):
         # fp16 and bf16 have the same dense tensor rate (kind::f16)
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+        kname = "bwd_kernel" if args.pass_ == "bwd" else "fwd_bf16_kernel"
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                    "frac": achieved / peak, "traffic": profiled_traffic(w.name, kname),
                     "peak_kind": f"{peak_kind} dense bf16 (burst)",
-                    "kernel": "bwd_kernel" if args.pass_ == "bwd" else "fwd_bf16_kernel",
-                    "flops_per_launch": flops}
+                    "kernel": kname, "flops_per_launch": flops}
     else:
         # fp32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 flops x max SM clock
         peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                    "frac": achieved / peak, "traffic": profiled_traffic(w.name, "fwd_fp32_kernel"),
                     "peak_kind": "fp32 FMA, derived from unit counts and max clock",
                     "kernel": "fwd_fp32_kernel", "flops_per_launch": flops}
     hbm_bytes = input_bytes + o.numel() * o.element_size() + lse.numel() * 4

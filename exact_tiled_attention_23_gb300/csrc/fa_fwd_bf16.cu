@@ -283,7 +283,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int64_t lim = p.causal ? (L < row + 1 ? L : row + 1) : L;   // visible keys: j < lim
         const float sl2 = p.scale_log2;
 
-        float m_ref = -INFINITY;   // running max of scale*log2e*S (possibly stale by <= 8)
+        float m_ref = -INFINITY;   // reference max of scale*log2e*S: a lower bound of the running max, raised lazily (below)
         float l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
