@@ -71,9 +71,12 @@ def measured_peaks():
 # The sources each timed kernel is built from; a DRAM-traffic figure taken
 # by ncu stays valid only while these files are unchanged.
 KERNEL_SOURCES = {
-    "fwd_bf16_kernel": ("fa_fwd_bf16.cu", "fa_tc_common.cuh", "sm103_ptx.cuh", "fa_internal.h", "fa_api.cu"),
+    "fwd_bf16_kernel": ("fa_fwd_bf16.cu", "fa_fwd_softmax.cuh", "fa_tc_common.cuh", "sm103_ptx.cuh",
+                        "fa_internal.h", "fa_api.cu"),
     "bwd_kernel": ("fa_bwd_bf16.cu", "fa_tc_common.cuh", "sm103_ptx.cuh", "fa_internal.h", "fa_api.cu"),
     "fwd_fp32_kernel": ("fa_fwd_fp32.cu", "fa_internal.h", "fa_api.cu"),
+    "fwd_d256_kernel": ("fa_fwd_d256.cu", "fa_fwd_softmax.cuh", "fa_tc_common.cuh", "sm103_ptx.cuh",
+                        "fa_internal.h", "fa_api.cu"),
 }
 
 
@@ -263,7 +266,7 @@ def run_ours(args, rank, world, local):
         torch.distributed.init_process_group("nccl", device_id=dev)
     fa.build()
     fa.load()
-    inp = workloads.make(args.workload, heads=args.heads, dtype=args.dtype, seq=args.seq)
+    inp = workloads.make(args.workload, heads=args.heads, dtype=args.dtype, seq=args.seq, dim=args.dim)
     w = inp.workload
     B, H, N, D = w.B, w.H, w.N, w.D
     pairs = workloads.unmasked_pairs(N, w.causal, None if inp.kv_len is None else inp.kv_len.tolist(), B, H)
@@ -363,7 +366,7 @@ def run_ours(args, rank, world, local):
     if w.dtype in ("bf16", "fp16"):
         # fp16 and bf16 have the same dense tensor rate (kind::f16)
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
-        kname = "bwd_kernel" if args.pass_ == "bwd" else "fwd_bf16_kernel"
+        kname = "bwd_kernel" if args.pass_ == "bwd" else "fwd_d256_kernel" if D == 256 else "fwd_bf16_kernel"
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name, kname),
                     "peak_kind": f"{peak_kind} dense bf16 (burst)",
@@ -464,6 +467,8 @@ def main():
                     help="write a 256 MiB buffer before every timed step (auto: when Q,K,V fit in 2x L2)")
     ap.add_argument("--seq", type=int, default=None,
                     help="override the workload's sequence length N (IO probe, profiler captures)")
+    ap.add_argument("--dim", type=int, default=None,
+                    help="override the workload's head dimension D")
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
                     help="override the element type of a 16-bit workload")
     ap.add_argument("--splits", type=int, default=None,

@@ -174,8 +174,8 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
             return_lse: bool = True, stream=None, splits=None, workspace=None):
     """O, LSE = attention(q, k, v) for CUDA tensors of shape [B, H, N, D].
 
-    bf16 and fp16 inputs use the tensor-core path (D in {64, 128}); fp32
-    inputs use the fp32 path (D <= 256).  scale=None selects 1/sqrt(D).  kv_len: optional
+    bf16 and fp16 inputs use the tensor-core path (D a multiple of 8 up to
+    128, or 256); fp32 inputs use the fp32 path (D <= 256).  scale=None selects 1/sqrt(D).  kv_len: optional
     int32 CUDA tensor [B] of key lengths.  Runs asynchronously on `stream`
     (default: torch's current stream).
 

@@ -50,6 +50,10 @@ uint64_t wait_limit_ns()
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Head dimensions of the split-capable tensor-core forward: multiples of 8
+// (a TMA row stride must be a multiple of 16 bytes) up to 128.
+bool tc_fwd_head_dim(int D) { return D > 0 && D <= 128 && D % 8 == 0; }
+
 fa_status check_common(const void *Q, const void *K, const void *V, const void *O, int B, int H,
                        int N, int D)
 {
@@ -139,11 +143,14 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
     fa_status st = check_common(Q, K, V, O, B, H, N, D);
     if (st != FA_OK) return st;
     if ((int64_t)B * H * N == 0) return FA_OK;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!tc_fwd_head_dim(D) && D != 256) return FA_ERR_UNSUPPORTED;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
     if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
     if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
-    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    // one work item covers 256 query rows of one head (128 for D = 256); the
+    // grid is 1-D
+    const int64_t rows_per_item = D == 256 ? 128 : 256;
+    const int64_t items = (int64_t)B * H * (((int64_t)N + rows_per_item - 1) / rows_per_item);
     if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
     const int64_t BH = (int64_t)B * H;
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -153,7 +160,8 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
         return FA_ERR_CUDA;
     fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
     p.f16 = f16 ? 1 : 0;
-    cudaError_t e = fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    cudaError_t e = D == 256 ? fa::launch_fwd_d256(p, tq, tk, tv, static_cast<cudaStream_t>(stream))
+                             : fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -170,25 +178,7 @@ fa_status fa_fwd_f16(const void *Q, const void *K, const void *V, void *O, float
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                  int N, int D, int causal, float scale, const int32_t *kv_len, void *stream)
 {
-    fa_status st = check_common(Q, K, V, O, B, H, N, D);
-    if (st != FA_OK) return st;
-    if ((int64_t)B * H * N == 0) return FA_OK;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
-    if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
-    if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
-    // one work item covers 256 query rows of one head; the grid is 1-D
-    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
-    if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
-
-    const int64_t BH = (int64_t)B * H;
-    CUtensorMap tq, tk, tv;
-    if (!encode_bf16_map(&tq, Q, BH, N, D) || !encode_bf16_map(&tk, K, BH, N, D) ||
-        !encode_bf16_map(&tv, V, BH, N, D))
-        return FA_ERR_CUDA;
-    const fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
-    cudaError_t e = fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return fwd16(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream, false);
 }
 
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits)
@@ -223,7 +213,7 @@ fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, f
     fa_status st = check_common(Q, K, V, O, B, H, N, D);
     if (st != FA_OK) return st;
     if ((int64_t)B * H * N == 0) return FA_OK;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!tc_fwd_head_dim(D)) return FA_ERR_UNSUPPORTED;
     if (num_splits < 0 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
     if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
@@ -336,11 +326,11 @@ const char *fa_status_string(fa_status s)
 
 fa_status fa_device_status(void *stream)
 {
-    uint32_t v = 0, vb = 0;
+    uint32_t v = 0, vb = 0, vd = 0;
     if (fa::read_and_clear_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess ||
-        fa::read_and_clear_status_bwd(&vb) != cudaSuccess)
+        fa::read_and_clear_status_bwd(&vb) != cudaSuccess || fa::read_and_clear_status_d256(&vd) != cudaSuccess)
         return FA_ERR_CUDA;
-    v |= vb;
+    v |= vb | vd;
     if (v) {
         g_last_detail = v;
         if (v & fa::kStatusTimeout) return FA_ERR_TIMEOUT;

@@ -33,6 +33,7 @@
 // Every mbarrier wait is bounded by a time budget; a wait that runs out sets
 // the library's device status word, raises a CTA-wide abort flag, and every
 // role then drains its in-flight copies / MMAs, frees tensor memory and exits.
+#include "fa_fwd_softmax.cuh"
 #include "fa_internal.h"
 #include "fa_tc_common.cuh"
 #include "sm103_ptx.cuh"
@@ -49,12 +50,6 @@ constexpr int BM = 128;          // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;          // keys per step
 constexpr int kThreads = 384;    // 12 warps
 constexpr int kFirstSoftmaxWarp = 4;
-// Largest block sum of p kept without a max scan: 2^64.  It bounds every p
-// by 2^64, so l <= N * 2^64 and |O| <= N * 2^64 * max|V| stay far below the
-// fp32/bf16 limit of ~2^128 for any N < 2^31 and max|V| < 2^30.
-constexpr float kLazyLimit = 18446744073709551616.f;
-// With fp16 operands P must also fit fp16 (max 65504): every p <= 2^15.
-constexpr float kLazyLimitF16 = 32768.f;
 
 template <int D>
 struct Layout {
@@ -283,8 +278,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int64_t lim = p.causal ? (L < row + 1 ? L : row + 1) : L;   // visible keys: j < lim
         const float sl2 = p.scale_log2;
 
-        float m_ref = -INFINITY;   // reference max of scale*log2e*S: a lower bound of the running max, raised lazily (below)
-        float l = 0.f;
+        OnlineRow<D, kF16> st;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const bool got = wait_bounded(&s_full[i], j & 1, p.wait_limit_ns, kSiteSFull, ab);
@@ -306,90 +300,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int t = 0; t < 32; ++t)
                         if (c * 32 + t >= vis) s_raw[c][t] = f2u(-INFINITY);
             }
-            // Reference max m_ref.  The first key block sets it from the row
-            // max.  Later blocks reuse it without scanning for their max as
-            // long as the block's sum of p stays <= kLazyLimit, which bounds
-            // every p (l, P and O stay far from overflow); a block that
-            // exceeds that, or gives inf/NaN, scans its max, raises m_ref,
-            // rescales O and l by 2^(m_old - m_new) and recomputes P.  l and O
-            // always share m_ref, so the result is exact in real arithmetic.
-            auto raise_reference = [&]() {
-                float mx8[8];
-#pragma unroll
-                for (int a = 0; a < 8; ++a) mx8[a] = u2f(s_raw[0][a]);
-#pragma unroll
-                for (int k = 8; k < 128; k += 16)
-#pragma unroll
-                    for (int a = 0; a < 8; ++a)
-                        mx8[a] = ptx::max3(mx8[a], u2f(s_raw[(k + 2 * a) / 32][(k + 2 * a) % 32]),
-                                           u2f(s_raw[(k + 2 * a + 1) / 32][(k + 2 * a + 1) % 32]));
-                const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
-                                       fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                const float m_new = fmaxf(m_ref, mx * sl2);
-                const float alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2_approx(m_ref - m_new);
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    const uint64_t a2 = ptx::pack2(alpha, alpha);
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        ptx::tmem_ld32(tO + c * 32, o);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            float lo, hi;
-                            ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])), a2), lo, hi);
-                            o[2 * t] = f2u(lo);
-                            o[2 * t + 1] = f2u(hi);
-                        }
-                        ptx::tmem_st32(tO + c * 32, o);
-                    }
-                }
-                l *= alpha;
-                m_ref = m_new;
-            };
-            // p = 2^(S*scale*log2e - m_ref): packed FMA, MUFU ex2, packed sums;
-            // P goes back over the first 64 columns of S as bf16 pairs.
-            auto exp_pass = [&]() -> float {
-                const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                const uint64_t t2 = ptx::pack2(sl2, sl2);
-                const uint64_t nm2 = ptx::pack2(-mref_use, -mref_use);
-                uint64_t acc2[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) acc2[a] = 0ull;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        float y0, y1;
-                        ptx::unpack2(ptx::fma2(ptx::pack2(u2f(s_raw[c][2 * t]), u2f(s_raw[c][2 * t + 1])), t2, nm2),
-                                     y0, y1);
-                        const float p0 = ptx::ex2_approx(y0);
-                        const float p1 = ptx::ex2_approx(y1);
-                        acc2[t & 3] = ptx::add2(acc2[t & 3], ptx::pack2(p0, p1));
-                        pk[t] = ptx::pack16x2<kF16>(p0, p1);
-                    }
-                    ptx::tmem_st16(tS + c * 16, pk);
-                }
-                float a0, a1, b0, b1, c0, c1, d0, d1;
-                ptx::unpack2(acc2[0], a0, a1);
-                ptx::unpack2(acc2[1], b0, b1);
-                ptx::unpack2(acc2[2], c0, c1);
-                ptx::unpack2(acc2[3], d0, d1);
-                return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-            };
-            if (__any_sync(0xffffffffu, m_ref == -INFINITY)) raise_reference();
-            float sum = exp_pass();
-            if (__any_sync(0xffffffffu, !(sum <= (kF16 ? kLazyLimitF16 : kLazyLimit)))) {
-                raise_reference();
-                ptx::tmem_wait_st();      // the first pass's P stores land before the new ones
-                sum = exp_pass();
-            }
-            ptx::tmem_wait_st();
-            l += sum;
+            // O_i is never being written here: s_full[i] for block j is
+            // committed after PV_i of block j-1.
+            st.block(s_raw, sl2, j > 0, tS, tO, [] {});
             ptx::tc_fence_before();
             ptx::mbar_arrive(&p_full[i]);
         }
+        const float l = st.l, m_ref = st.m_ref;
 
         // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----------------
         bool have = (n_kv > 0) && ok;
@@ -402,11 +319,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const bool empty = !(l > 0.f);
             const float inv = empty ? 0.f : 1.f / l;
             const float lse_row = empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
+            // Only the first p.D (a multiple of 8, <= D) columns exist in
+            // memory; the rest of the D computed ones are the zero padding.
+            const int Dv = (int)p.D;
             const int64_t flat = bh * N + row;
-            uint16_t *orow = static_cast<uint16_t *>(p.o) + flat * D;
-            float *prow = kSplit ? p.part_o + ((int64_t)split * BH * N + flat) * D : nullptr;
+            uint16_t *orow = static_cast<uint16_t *>(p.o) + flat * Dv;
+            float *prow = kSplit ? p.part_o + ((int64_t)split * BH * N + flat) * Dv : nullptr;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 32 && c * 32 < Dv; ++c) {
                 uint32_t o[32];
                 if (n_kv > 0) {
                     ptx::tmem_ld32(tO + c * 32, o);
@@ -429,12 +349,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         float4 *dst = reinterpret_cast<float4 *>(prow + c * 32);
 #pragma unroll
                         for (int t = 0; t < 8; ++t)
-                            dst[t] = make_float4(f[4 * t], f[4 * t + 1], f[4 * t + 2], f[4 * t + 3]);
+                            if (c * 32 + 4 * t < Dv)
+                                dst[t] = make_float4(f[4 * t], f[4 * t + 1], f[4 * t + 2], f[4 * t + 3]);
                     } else {
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                         for (int t = 0; t < 4; ++t)
-                            dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                            if (c * 32 + 8 * t < Dv)
+                                dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                     }
                 }
             }
@@ -479,16 +401,20 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
 // normalised output O_s and LSE_s over its key range; with m = max_s LSE_s and
 // w_s = exp(LSE_s - m): O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s.
 // Ranges with no visible key have LSE_s = -inf and weight 0; a row with none
-// at all gets O = +0 and LSE = -inf.  One warp per row, D/32 columns per lane.
+// at all gets O = +0 and LSE = -inf.  One warp per row, D/32 columns per lane
+// (D = the padded head dimension; lanes past the Dv real columns only help
+// with the LSE).
 template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
 merge_splits_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
-                    uint16_t *__restrict__ out, float *__restrict__ lse, int64_t rows, int splits)
+                    uint16_t *__restrict__ out, float *__restrict__ lse, int64_t rows, int splits,
+                    int Dv)
 {
     constexpr int kPer = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
+    const bool cols = lane * kPer < Dv;   // Dv is a multiple of 8: a lane's columns are all in or all out
     float m = -INFINITY;
     for (int s = 0; s < splits; ++s) m = fmaxf(m, part_lse[(int64_t)s * rows + row]);
     float acc[kPer];
@@ -501,7 +427,8 @@ merge_splits_kernel(const float *__restrict__ part_o, const float *__restrict__ 
             if (!(ls > -INFINITY)) continue;
             const float w = expf(ls - m);
             wsum += w;
-            const float *src = part_o + ((int64_t)s * rows + row) * D + lane * kPer;
+            if (!cols) continue;
+            const float *src = part_o + ((int64_t)s * rows + row) * Dv + lane * kPer;
             if constexpr (kPer == 4) {
                 const float4 v = *reinterpret_cast<const float4 *>(src);
                 acc[0] = fmaf(w, v.x, acc[0]);
@@ -521,11 +448,13 @@ merge_splits_kernel(const float *__restrict__ part_o, const float *__restrict__ 
 #pragma unroll
     for (int c = 0; c < kPer / 2; ++c)
         packed[c] = empty ? 0u : ptx::pack16x2<kF16>(acc[2 * c] * inv, acc[2 * c + 1] * inv);
-    uint16_t *dst = out + row * D + lane * kPer;
-    if constexpr (kPer == 4)
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-    else
-        *reinterpret_cast<uint32_t *>(dst) = packed[0];
+    uint16_t *dst = out + row * Dv + lane * kPer;
+    if (cols) {
+        if constexpr (kPer == 4)
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+        else
+            *reinterpret_cast<uint32_t *>(dst) = packed[0];
+    }
     if (lse && lane == 0) lse[row] = empty ? -INFINITY : m + logf(wsum);
 }
 
@@ -537,31 +466,34 @@ cudaError_t launch_split(const FwdParams &p, const CUtensorMap &tq, const CUtens
     if (e != cudaSuccess) return e;
     const int64_t rows = p.B * p.H * p.N;
     merge_splits_kernel<D, kF16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        p.part_o, p.part_lse, static_cast<uint16_t *>(p.o), p.lse, rows, p.num_splits);
+        p.part_o, p.part_lse, static_cast<uint16_t *>(p.o), p.lse, rows, p.num_splits, (int)p.D);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+// A head dimension D that is a multiple of 8 runs in the kernel for the next
+// of 64 / 128: the TMA boxes (64 columns) fill the columns past D with zeros,
+// which leaves every score unchanged, and the padded output columns are never
+// stored.
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, cudaStream_t stream)
 {
-    if (p.D == 64)
+    if (p.D % 8 != 0 || p.D <= 0 || p.D > 128) return cudaErrorInvalidValue;
+    if (p.D <= 64)
         return p.f16 ? launch_d<64, false, true>(p, tm_q, tm_k, tm_v, stream)
                      : launch_d<64, false, false>(p, tm_q, tm_k, tm_v, stream);
-    if (p.D == 128)
-        return p.f16 ? launch_d<128, false, true>(p, tm_q, tm_k, tm_v, stream)
-                     : launch_d<128, false, false>(p, tm_q, tm_k, tm_v, stream);
-    return cudaErrorInvalidValue;
+    return p.f16 ? launch_d<128, false, true>(p, tm_q, tm_k, tm_v, stream)
+                 : launch_d<128, false, false>(p, tm_q, tm_k, tm_v, stream);
 }
 
 cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                   const CUtensorMap &tm_v, cudaStream_t stream)
 {
     if (p.f16) return cudaErrorInvalidValue;   // the split-KV path is bf16 only
-    if (p.D == 64) return launch_split<64, false>(p, tm_q, tm_k, tm_v, stream);
-    if (p.D == 128) return launch_split<128, false>(p, tm_q, tm_k, tm_v, stream);
-    return cudaErrorInvalidValue;
+    if (p.D % 8 != 0 || p.D <= 0 || p.D > 128) return cudaErrorInvalidValue;
+    if (p.D <= 64) return launch_split<64, false>(p, tm_q, tm_k, tm_v, stream);
+    return launch_split<128, false>(p, tm_q, tm_k, tm_v, stream);
 }
 
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out)

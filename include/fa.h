@@ -63,7 +63,15 @@ typedef enum fa_status {
  *            attention-kernel", Key design decisions 4).
  *   B, H, N  batch, heads, sequence length; any value >= 0.  B*H*N == 0
  *            returns FA_OK without a launch.
- *   D        head dimension: 64 or 128 (others give FA_ERR_UNSUPPORTED).
+ *   D        head dimension: a multiple of 8 from 8 to 128, or 256 (the
+ *            pages run D = 16 in "vectorized-flash-attention-kernel",
+ *            Evidence & signatures, and d = 32 in "js-flash-attention-tiled-
+ *            online-softmax-exactness", Verification).  Other values give
+ *            FA_ERR_UNSUPPORTED.  Below 128 the tensor cores run at D
+ *            rounded up to 64 or 128 with zero-filled columns, which leave
+ *            every score unchanged; only the D real columns of O are
+ *            written.  D = 256 has a kernel of its own (one 128-row query
+ *            tile per CTA).
  *   causal   nonzero: key j is hidden from query i when j > i.
  *   scale    softmax scale; NaN or <= 0 selects the default 1/sqrt(D)
  *            ("vectorized-flash-attention-kernel", Constructor options).
@@ -118,6 +126,7 @@ fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, 
  *                    bytes; its contents on entry do not matter, it is fully
  *                    rewritten, and it must not be used by another call that
  *                    may run at the same time.
+ * D is a multiple of 8 up to 128 (256 gives FA_ERR_UNSUPPORTED here).
  * Returns FA_ERR_INVALID_ARG for a missing, misaligned or too small
  * workspace or a split count out of range; otherwise as fa_fwd.
  */

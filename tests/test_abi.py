@@ -66,9 +66,11 @@ def test_null_and_negative_arguments(lib, fn):
     assert fn(P, P, P, P, None, 1, 1, 16, 0, 1, NAN, None, None) == fa.FA_ERR_INVALID_ARG
 
 
-def test_bf16_head_dims(lib):
-    for D in (16, 32, 96, 192, 256):
-        assert fa.fa_fwd(P, P, P, P, None, 1, 1, 16, D, 1, NAN, None, None) == fa.FA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("fn", [fa.fa_fwd, fa.fa_fwd_f16])
+def test_tensor_core_head_dims(lib, fn):
+    # multiples of 8 up to 128 run; the rest is rejected before any CUDA call
+    for D in (4, 12, 100, 129, 136, 192, 264):
+        assert fn(P, P, P, P, None, 1, 1, 16, D, 1, NAN, None, None) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_fp32_head_dim_limit(lib):
@@ -112,7 +114,8 @@ def test_splitkv_argument_checks(lib):
     assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, fa.FA_MAX_SPLITS + 1, P, big, None) == fa.FA_ERR_INVALID_ARG
     need = fa.fa_fwd_splitkv_workspace_bytes(1, 1, 16, 64, 2)
     assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 64, 1, NAN, None, 2, P, need - 1, None) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 96, 1, NAN, None, 2, P, big, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 100, 1, NAN, None, 2, P, big, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_splitkv(P, P, P, P, None, 1, 1, 16, 256, 1, NAN, None, 2, P, big, None) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fwd_splitkv(None, None, None, None, None, 1, 1, 0, 64, 1, NAN, None, 2, None, 0, None) == fa.FA_OK
 
 

@@ -222,6 +222,82 @@ def test_f16_large_logits():
     compare(inp, o, lse)
 
 
+HEAD_DIM_CASES = [
+    # B, H, N, D, dtype, causal, kv_len: head dims other than 64 / 128 (zero
+    # padded to the next of 64 / 128 below 128; D = 256 has its own kernel)
+    (1, 2, 200, 8, "bf16", True, None),
+    (2, 1, 130, 16, "bf16", False, [130, 7]),
+    (1, 2, 300, 32, "bf16", True, None),
+    (1, 1, 257, 40, "bf16", False, None),
+    (2, 2, 384, 96, "bf16", True, [384, 0]),
+    (1, 2, 513, 112, "bf16", False, None),
+    (1, 1, 1, 256, "bf16", True, None),
+    (1, 2, 127, 256, "bf16", True, None),
+    (2, 2, 300, 256, "bf16", False, [300, 0]),
+    (1, 2, 1024, 256, "bf16", True, [1000]),
+    (1, 1, 640, 256, "bf16", False, None),
+    (1, 2, 300, 32, "fp16", True, None),
+    (2, 1, 257, 96, "fp16", False, [200, 257]),
+    (1, 2, 513, 256, "fp16", True, None),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,dtype,causal,kv_len", HEAD_DIM_CASES)
+def test_head_dims(B, H, N, D, dtype, causal, kv_len):
+    inp = workloads.make_case(B, H, N, D, dtype=dtype, causal=causal, seed=N + 3 * D, kv_len=kv_len)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
+@pytest.mark.parametrize("D", [32, 96, 256])
+def test_head_dim_writes_stay_in_bounds(D):
+    """O is written through a view of a larger buffer: nothing past the last
+    row's D columns changes (the padded columns are never stored)."""
+    B, H, N = 1, 2, 300
+    inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=True, seed=D)
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    n = B * H * N * D
+    buf = torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[:n].view(B, H, N, D)
+    o, lse = fa.forward(q, k, v, causal=True, out=out)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    assert torch.all(buf[n:] == 7.0)
+    compare(inp, o, lse)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_d256_growing_logits(causal):
+    """D = 256: key magnitudes ramp x1 -> x60, so later key blocks keep
+    raising the row max and O is rescaled while the previous block's P V may
+    still be in flight (the rescale waits for it)."""
+    inp = workloads.make_case(1, 2, 1024, 256, dtype="bf16", causal=causal, seed=19)
+    ramp = torch.linspace(1.0, 60.0, 1024)[None, None, :, None]
+    inp.k = (inp.k.float() * ramp).to(torch.bfloat16)
+    q = inp.q.float()
+    q[:, :, ::3] *= 3.0
+    inp.q = q.to(torch.bfloat16)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
+SPLIT_HEAD_DIM_CASES = [
+    (1, 2, 1024, 32, True, None, 3),
+    (2, 1, 700, 96, False, [700, 90], 2),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len,splits", SPLIT_HEAD_DIM_CASES)
+def test_splitkv_head_dims(B, H, N, D, causal, kv_len, splits):
+    inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=causal, seed=N + D + splits, kv_len=kv_len)
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    kv = inp.kv_len.cuda() if inp.kv_len is not None else None
+    o, lse = fa.forward(q, k, v, causal=causal, kv_len=kv, splits=splits)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    compare(inp, o, lse)
+
+
 FP32_CASES = [
     (1, 1, 1, 16, True, None),
     (1, 2, 128, 64, True, None),

@@ -122,19 +122,20 @@ def draw(B: int, H: int, N: int, D: int, dtype: str, seed: int, *, padded: str =
 
 
 def make(name: str, heads: Optional[int] = None, dtype: Optional[str] = None,
-         seq: Optional[int] = None) -> Inputs:
-    """Inputs of a named workload (see WORKLOADS).  `heads` and `seq`
-    override H and N (a resized copy of the same workload, e.g. for profiler
-    captures and the IO probe) and `dtype` the element type of a 16-bit
-    workload ("bf16" or "fp16")."""
+         seq: Optional[int] = None, dim: Optional[int] = None) -> Inputs:
+    """Inputs of a named workload (see WORKLOADS).  `heads`, `seq` and `dim`
+    override H, N and D (a resized copy of the same workload, e.g. for
+    profiler captures, the IO probe and other head dimensions) and `dtype` the
+    element type of a 16-bit workload ("bf16" or "fp16")."""
     w = WORKLOADS[name]
     H = w.H if heads is None else int(heads)
     N = w.N if seq is None else int(seq)
+    D = w.D if dim is None else int(dim)
     dt = w.dtype if dtype is None else dtype
-    if (H, N, dt) != (w.H, w.N, w.dtype):
+    if (H, N, D, dt) != (w.H, w.N, w.D, w.dtype):
         suffix = (f"_h{H}" if H != w.H else "") + (f"_n{N}" if N != w.N else "") + \
-                 (f"_{dt}" if dt != w.dtype else "")
-        w = Workload(f"{w.name}{suffix}", w.index, dt, w.B, H, N, w.D, w.causal,
+                 (f"_d{D}" if D != w.D else "") + (f"_{dt}" if dt != w.dtype else "")
+        w = Workload(f"{w.name}{suffix}", w.index, dt, w.B, H, N, D, w.causal,
                      padded=w.padded, spiky_rows=w.spiky_rows, spike=w.spike, note=w.note)
     q, k, v, lens, spiky = draw(w.B, w.H, w.N, w.D, w.dtype, w.seed, padded=w.padded,
                                 spiky_rows=w.spiky_rows, spike=w.spike)
