@@ -40,8 +40,9 @@ namespace {
 
 constexpr int BK = 128;              // keys per CTA (= TMEM lanes of S^T, dP^T, dK, dV)
 constexpr int BQ = 128;              // query rows per step
-constexpr int kThreads = 256;        // warp 0 TMA, warp 1 MMA, warps 4-7 key/query rows
+constexpr int kThreads = 384;        // warp 0 TMA, warp 1 MMA, warps 4-7 key rows, warps 8-11 query rows
 constexpr int kWorkWarp0 = 4;
+constexpr int kDQWarp0 = 8;
 
 template <int D>
 struct BwdLayout {
@@ -74,20 +75,22 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bars[12];
+    __shared__ uint64_t bars[14];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_word;
-    __shared__ __align__(16) float lse2_s[BQ];     // LSE of the current query tile, log2 units (+inf: no row)
-    __shared__ __align__(16) float delta_s[BQ];    // Delta of the current query tile
+    __shared__ __align__(16) float nlse2_s[BQ];    // -LSE of the current query tile, log2 units (-inf: no row)
+    __shared__ __align__(16) float ndelta_s[BQ];   // -Delta of the current query tile
     uint64_t *kv_full = &bars[0];
     uint64_t *stage_full = &bars[1];   // [2]
     uint64_t *stage_empty = &bars[3];  // [2]
-    uint64_t *s_full = &bars[5];
-    uint64_t *p_ready = &bars[6];
-    uint64_t *dq_full = &bars[7];
-    uint64_t *dq_free = &bars[8];
-    uint64_t *acc_full = &bars[9];
-    uint64_t *mma_drain = &bars[10];
+    uint64_t *s_full = &bars[5];       // S^T, dP^T in TMEM
+    uint64_t *p_ready = &bars[6];      // P^T, dS^T (bf16) in TMEM
+    uint64_t *ds_ready = &bars[7];     // dS in shared memory
+    uint64_t *dq_full = &bars[8];      // dQ_i in TMEM
+    uint64_t *dq_free = &bars[9];      // dQ_i read out of TMEM
+    uint64_t *ds_free = &bars[10];     // the dQ staging no longer reads the dS buffer
+    uint64_t *acc_full = &bars[11];
+    uint64_t *mma_drain = &bars[12];
     const Abort ab{&abort_word, &g_status_bwd};
 
     const int warp = threadIdx.x >> 5;
@@ -116,8 +119,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         ptx::mbar_init(s_full, 1);
         ptx::mbar_init(p_ready, 128);
+        ptx::mbar_init(ds_ready, 128);
         ptx::mbar_init(dq_full, 1);
         ptx::mbar_init(dq_free, 128);
+        ptx::mbar_init(ds_free, 1);
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(mma_drain, 1);
         abort_word = 0;
@@ -132,6 +137,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
+    // Registers: the TMA / MMA warpgroup needs few; the two row warpgroups
+    // hold a 64-column slice of S^T and dP^T, or a 128-column dQ row.
+    // 128*112 + 2*128*192 fits in the 384*168 registers of the launch.
+    if (warp < kWorkWarp0) {
+    ptx::regs_dec<112>();
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && n_iter > 0) {
@@ -191,6 +201,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 const uint64_t dQ_mn = make_sdesc(st, Lay::kChunkBytes, 1024);
                 const uint64_t dO_mn = make_sdesc(st + Lay::kTileBytes, Lay::kChunkBytes, 1024);
                 if (!wait_bounded(&stage_full[s], (it >> 1) & 1, p.wait_limit_ns, kSiteSlotFull, ab)) break;
+                // dQ_{i-1} has left the S^T columns
                 if (it > 0 && !wait_bounded(dq_free, (it - 1) & 1, p.wait_limit_ns, kSitePFull, ab)) break;
                 ptx::tc_fence_after();
 #pragma unroll
@@ -218,22 +229,26 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDPT + k * 8, dQ_mn + off, id_acc,
                                 (it > 0 || k > 0) ? 1u : 0u);
                 }
+                ptx::mma_commit(&stage_empty[s]);     // Q_i, dO_i are no longer read
+                if (!wait_bounded(ds_ready, it & 1, p.wait_limit_ns, kSitePFull, ab)) break;
+                ptx::tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint64_t off = (uint64_t)((k * 2048) >> 4);
                     ptx::mma_ss(tmem + Lay::kColST, dS_mn + off, dK_mn + off, id_dq, k > 0);
                 }
                 ptx::mma_commit(dq_full);
-                ptx::mma_commit(&stage_empty[s]);
                 if (it + 1 == n_iter) ptx::mma_commit(acc_full);
             }
             ptx::mma_commit(mma_drain);
             wait_bounded(mma_drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
         }
-    } else if (warp >= kWorkWarp0) {
-        // ================= key rows: P^T, dS^T; query rows: dQ =================
+    }
+    } else if (warp < kDQWarp0) {
+        ptx::regs_inc<192>();
+        // ================= key rows: P^T, dS^T =================
         const int quarter = warp & 3;
-        const int t = quarter * 32 + lane;                      // TMEM lane: key t (and query t for dQ)
+        const int t = quarter * 32 + lane;                      // TMEM lane: key t
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int64_t key = k0 + t;
         const bool key_ok = key < L;
@@ -242,12 +257,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         bool ok = true;
         for (int it = 0; it < n_iter && ok; ++it) {
             const int64_t q0 = (i0 + it) * BQ;
-            // this query tile's LSE (log2 units) and Delta, shared by all key rows
+            // this query tile's -LSE (log2 units) and -Delta, shared by all key rows
             ptx::bar_sync(1, 128);
             {
                 const int64_t qr = q0 + t;
-                lse2_s[t] = qr < N ? p.lse[bh * N + qr] * 1.4426950408889634f : INFINITY;
-                delta_s[t] = qr < N ? p.delta[bh * N + qr] : 0.f;
+                nlse2_s[t] = qr < N ? p.lse[bh * N + qr] * -1.4426950408889634f : -INFINITY;
+                ndelta_s[t] = qr < N ? -p.delta[bh * N + qr] : 0.f;
             }
             ptx::bar_sync(1, 128);
             // all 128 threads agree on going on, so the named barriers stay matched
@@ -260,15 +275,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 ptx::tmem_ld32(tmem + lane_off + Lay::kColST + c * 32, sv);
                 ptx::tmem_ld32(tmem + lane_off + Lay::kColDPT + c * 32, dpv);
                 ptx::tmem_wait_ld();
-                // this chunk's 32 LSE / Delta values (broadcast smem reads) and the
-                // first visible query: causal hides q < key, padding hides the row
-                float lse_c[32], dl_c[32];
+                // this chunk's 32 -LSE / -Delta values as packed pairs (broadcast
+                // smem reads) and the first visible query: causal hides q < key,
+                // padding hides the row
+                uint64_t nl2[16], nd2[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(&lse2_s[c * 32 + e]);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(&delta_s[c * 32 + e]);
-                    lse_c[e] = a4.x; lse_c[e + 1] = a4.y; lse_c[e + 2] = a4.z; lse_c[e + 3] = a4.w;
-                    dl_c[e] = d4.x; dl_c[e + 1] = d4.y; dl_c[e + 2] = d4.z; dl_c[e + 3] = d4.w;
+                for (int e = 0; e < 16; e += 2) {
+                    const ulonglong2 a2 = *reinterpret_cast<const ulonglong2 *>(&nlse2_s[c * 32 + 2 * e]);
+                    const ulonglong2 d2 = *reinterpret_cast<const ulonglong2 *>(&ndelta_s[c * 32 + 2 * e]);
+                    nl2[e] = a2.x; nl2[e + 1] = a2.y;
+                    nd2[e] = d2.x; nd2[e + 1] = d2.y;
                 }
                 int e_min = 0;
                 if (!key_ok) {
@@ -278,77 +294,64 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     e_min = d0 <= 0 ? 0 : (d0 >= 32 ? 32 : (int)d0);
                 }
                 uint32_t pw[16], dsw[16];
+                const uint64_t sl2_2 = ptx::pack2(sl2, sl2);
+                if (__all_sync(0xffffffffu, e_min == 0)) {
+                    // every query of the chunk sees every key of the warp: packed math
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float pa = e >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[e]), sl2, -lse_c[e])) : 0.f;
-                    const float pb = e + 1 >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[e + 1]), sl2, -lse_c[e + 1])) : 0.f;
-                    const float da = pa * (u2f(dpv[e]) - dl_c[e]);
-                    const float db = pb * (u2f(dpv[e + 1]) - dl_c[e + 1]);
-                    pw[e / 2] = ptx::pack_bf16x2(pa, pb);
-                    dsw[e / 2] = ptx::pack_bf16x2(da, db);
+                    for (int e = 0; e < 16; ++e) {
+                        float x0, x1, d0, d1;
+                        ptx::unpack2(ptx::fma2(ptx::pack2(u2f(sv[2 * e]), u2f(sv[2 * e + 1])), sl2_2, nl2[e]), x0, x1);
+                        const float p0 = ptx::ex2_approx(x0);
+                        const float p1 = ptx::ex2_approx(x1);
+                        ptx::unpack2(ptx::mul2(ptx::pack2(p0, p1),
+                                               ptx::add2(ptx::pack2(u2f(dpv[2 * e]), u2f(dpv[2 * e + 1])), nd2[e])),
+                                     d0, d1);
+                        pw[e] = ptx::pack_bf16x2(p0, p1);
+                        dsw[e] = ptx::pack_bf16x2(d0, d1);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float nla, nlb, nda, ndb;
+                        ptx::unpack2(nl2[e], nla, nlb);
+                        ptx::unpack2(nd2[e], nda, ndb);
+                        const float pa = 2 * e >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[2 * e]), sl2, nla)) : 0.f;
+                        const float pb = 2 * e + 1 >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, nlb)) : 0.f;
+                        pw[e] = ptx::pack_bf16x2(pa, pb);
+                        dsw[e] = ptx::pack_bf16x2(pa * (u2f(dpv[2 * e]) + nda), pb * (u2f(dpv[2 * e + 1]) + ndb));
+                    }
                 }
                 ptx::tmem_st16(tmem + lane_off + Lay::kColST + c * 16, pw);
                 ptx::tmem_st16(tmem + lane_off + Lay::kColDPT + c * 16, dsw);
-                // dS row of key t into the MN-major, 128-byte-swizzled A operand
-                // of dQ = dS K: query chunk c*32.. = 4 units of 8 queries
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int qq = c * 32 + w * 8;            // first query of the unit
-                    const uint32_t unit = (uint32_t)((qq % 64) / 8) ^ (uint32_t)(t & 7);
-                    const uint32_t addr = ds_base + (uint32_t)(qq / 64) * Lay::kChunkBytes + (uint32_t)t * 128u + (unit << 4);
-                    ptx::st_shared_v4(addr, dsw[4 * w], dsw[4 * w + 1], dsw[4 * w + 2], dsw[4 * w + 3]);
-                }
             }
             ptx::tmem_wait_st();
-            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(p_ready);
+            ptx::mbar_arrive(p_ready);      // dV += P^T dO_i and dK += dS^T Q_i may start
 
-            // dQ_i rows (TMEM lane t = query q0 + t) into the fp32 accumulator
-            ok = ptx::bar_and(1, 128, wait_bounded(dq_full, it & 1, p.wait_limit_ns, kSiteOFinal, ab));
-            if (!ok) break;
+            // dS (row t = key t) into the MN-major, 128-byte-swizzled A operand
+            // of dQ = dS K, once the staging of dQ_{i-1} has left the buffer;
+            // the bf16 pairs are read back from the dS^T columns of TMEM.
+            if (it > 0) {
+                ok = ptx::bar_and(1, 128, wait_bounded(ds_free, (it - 1) & 1, p.wait_limit_ns, kSitePFull, ab));
+                if (!ok) break;
+            }
             ptx::tc_fence_after();
-            // Each 32-column chunk of dQ_i (row t = query q0 + t) is staged in the
-            // dS buffer (free: dQ = dS K has read it) as a 128-row x 128-byte box
-            // with the 16-byte units of row r XOR-swizzled by (r & 7) -- the
-            // shared-memory form of a 128-byte-swizzled TMA box -- and one thread
-            // hands it to the TMA engine, which adds it into the fp32 accumulator
-            // (rows at or past N are clipped by the tensor map).
-            float *stage = reinterpret_cast<float *>(smem + Lay::kDSOff);
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                float *buf = stage + (c & 1) * (BQ * 32);
-                if (c >= 2) {
-                    // the reduce that read this buffer two chunks ago is done
-                    if (t == 0) ptx::bulk_wait_group_read<1>();
-                    ptx::bar_sync(1, 128);
-                }
-                uint32_t v[32];
-                ptx::tmem_ld32(tmem + lane_off + Lay::kColST + c * 32, v);
-                ptx::tmem_wait_ld();
-                if (c + 1 == D / 32) {
-                    // all of dQ_i is in registers or staged: TMEM may take the next S^T
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(dq_free);
-                }
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<uint4 *>(buf + t * 32 + ((e ^ (t & 7)) << 2)) =
-                        make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                ptx::fence_proxy_async_smem();
-                ptx::bar_sync(1, 128);
-                if (t == 0) {
-                    ptx::tma_reduce_add_3d(&tm_dq, buf, c * 32, (int32_t)q0, (int32_t)bh);
-                    ptx::bulk_commit_group();
+            for (int h = 0; h < BQ / 64; ++h) {
+                uint32_t dsv[32];
+                ptx::tmem_ld32(tmem + lane_off + Lay::kColDPT + h * 32, dsv);
+                ptx::tmem_wait_ld();
+                // 32 words = 64 queries = 8 units of 8 queries
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t unit = (uint32_t)u ^ (uint32_t)(t & 7);
+                    const uint32_t addr = ds_base + (uint32_t)h * Lay::kChunkBytes + (uint32_t)t * 128u + (unit << 4);
+                    ptx::st_shared_v4(addr, dsv[4 * u], dsv[4 * u + 1], dsv[4 * u + 2], dsv[4 * u + 3]);
                 }
             }
-            // the staging area is the next tile's dS buffer
-            if (t == 0) ptx::bulk_wait_group_read<0>();
-            ptx::bar_sync(1, 128);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(ds_ready);
         }
-
-        // every reduce-add this thread issued has reached global memory
-        if (t == 0) ptx::bulk_wait_group_all();
 
         // ---- dK (times scale) and dV of this key tile ------------------------
         bool have = ok && n_iter > 0;
@@ -382,6 +385,57 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 }
             }
         }
+    } else {
+        ptx::regs_inc<192>();
+        // ================= query rows: dQ_i into the fp32 accumulator =================
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;                      // TMEM lane: query q0 + t
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        float *stage = reinterpret_cast<float *>(smem + Lay::kDSOff);
+        for (int it = 0; it < n_iter; ++it) {
+            const int64_t q0 = (i0 + it) * BQ;
+            if (!ptx::bar_and(2, 128, wait_bounded(dq_full, it & 1, p.wait_limit_ns, kSiteOFinal, ab))) break;
+            ptx::tc_fence_after();
+            // dQ_i goes to registers first, so that TMEM is handed back to the
+            // next S^T at once.  Each 32-column chunk is then staged in the dS
+            // buffer (free: dQ = dS K has read it) as a 128-row x 128-byte box
+            // with the 16-byte units of row r XOR-swizzled by (r & 7) -- the
+            // shared-memory form of a 128-byte-swizzled TMA box -- and one
+            // thread hands it to the TMA engine, which adds it into the fp32
+            // accumulator (rows at or past N are clipped by the tensor map).
+            uint32_t dqv[D / 32][32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tmem + lane_off + Lay::kColST + c * 32, dqv[c]);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(dq_free);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float *buf = stage + (c & 1) * (BQ * 32);
+                if (c >= 2) {
+                    // the reduce that read this buffer two chunks ago is done
+                    if (t == 0) ptx::bulk_wait_group_read<1>();
+                    ptx::bar_sync(2, 128);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<uint4 *>(buf + t * 32 + ((e ^ (t & 7)) << 2)) =
+                        make_uint4(dqv[c][4 * e], dqv[c][4 * e + 1], dqv[c][4 * e + 2], dqv[c][4 * e + 3]);
+                ptx::fence_proxy_async_smem();
+                ptx::bar_sync(2, 128);
+                if (t == 0) {
+                    ptx::tma_reduce_add_3d(&tm_dq, buf, c * 32, (int32_t)q0, (int32_t)bh);
+                    ptx::bulk_commit_group();
+                }
+            }
+            // the buffer is the next tile's dS: hand it back once read
+            if (t == 0) {
+                ptx::bulk_wait_group_read<0>();
+                ptx::mbar_arrive(ds_free);
+            }
+        }
+        // every reduce-add issued here has reached global memory
+        if (t == 0) ptx::bulk_wait_group_all();
     }
 
     ptx::tc_fence_before();
