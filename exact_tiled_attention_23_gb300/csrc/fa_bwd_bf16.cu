@@ -75,7 +75,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bars[14];
+    __shared__ uint64_t bars[17];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_word;
     __shared__ __align__(16) float nlse2_s[BQ];    // -LSE of the current query tile, log2 units (-inf: no row)
@@ -84,13 +84,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     uint64_t *stage_full = &bars[1];   // [2]
     uint64_t *stage_empty = &bars[3];  // [2]
     uint64_t *s_full = &bars[5];       // S^T, dP^T in TMEM
-    uint64_t *p_ready = &bars[6];      // P^T, dS^T (bf16) in TMEM
-    uint64_t *ds_ready = &bars[7];     // dS in shared memory
-    uint64_t *dq_full = &bars[8];      // dQ_i in TMEM
-    uint64_t *dq_free = &bars[9];      // dQ_i read out of TMEM
-    uint64_t *ds_free = &bars[10];     // the dQ staging no longer reads the dS buffer
-    uint64_t *acc_full = &bars[11];
-    uint64_t *mma_drain = &bars[12];
+    uint64_t *ds_ready = &bars[6];     // dS in shared memory
+    uint64_t *dq_full = &bars[7];      // dQ_i in TMEM
+    uint64_t *dq_free = &bars[8];      // dQ_i read out of TMEM
+    uint64_t *ds_free = &bars[9];      // the dQ staging no longer reads the dS buffer
+    uint64_t *acc_full = &bars[10];
+    uint64_t *mma_drain = &bars[11];
+    uint64_t *p_ready = &bars[12];     // [BQ / 32]: P^T, dS^T (bf16) of 32 queries in TMEM
     const Abort ab{&abort_word, &g_status_bwd};
 
     const int warp = threadIdx.x >> 5;
@@ -118,7 +118,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             ptx::mbar_init(&stage_empty[s], 1);
         }
         ptx::mbar_init(s_full, 1);
-        ptx::mbar_init(p_ready, 128);
+        for (int c = 0; c < BQ / 32; ++c) ptx::mbar_init(&p_ready[c], 128);
         ptx::mbar_init(ds_ready, 128);
         ptx::mbar_init(dq_full, 1);
         ptx::mbar_init(dq_free, 128);
@@ -215,20 +215,23 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     ptx::mma_ss(tmem + Lay::kColDPT, dV_km + off, dO_km + off, id_st, k > 0);
                 }
                 ptx::mma_commit(s_full);
-                if (!wait_bounded(p_ready, it & 1, p.wait_limit_ns, kSitePFull, ab)) break;
-                ptx::tc_fence_after();
+                // dV += P^T dO_i and dK += dS^T Q_i, 32 queries (two K-steps)
+                // at a time as the key-row threads finish them
+                bool got = true;
 #pragma unroll
-                for (int k = 0; k < BQ / 16; ++k) {
-                    const uint64_t off = (uint64_t)((k * 2048) >> 4);
-                    ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColST + k * 8, dO_mn + off, id_acc,
-                                (it > 0 || k > 0) ? 1u : 0u);
-                }
+                for (int c = 0; c < BQ / 32; ++c) {
+                    if (!(got = wait_bounded(&p_ready[c], it & 1, p.wait_limit_ns, kSitePFull, ab))) break;
+                    ptx::tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < BQ / 16; ++k) {
-                    const uint64_t off = (uint64_t)((k * 2048) >> 4);
-                    ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDPT + k * 8, dQ_mn + off, id_acc,
-                                (it > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 2 * c; k < 2 * c + 2; ++k) {
+                        const uint64_t off = (uint64_t)((k * 2048) >> 4);
+                        ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColST + k * 8, dO_mn + off, id_acc,
+                                    (it > 0 || k > 0) ? 1u : 0u);
+                        ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDPT + k * 8, dQ_mn + off, id_acc,
+                                    (it > 0 || k > 0) ? 1u : 0u);
+                    }
                 }
+                if (!got) break;
                 ptx::mma_commit(&stage_empty[s]);     // Q_i, dO_i are no longer read
                 if (!wait_bounded(ds_ready, it & 1, p.wait_limit_ns, kSitePFull, ab)) break;
                 ptx::tc_fence_after();
@@ -323,10 +326,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 }
                 ptx::tmem_st16(tmem + lane_off + Lay::kColST + c * 16, pw);
                 ptx::tmem_st16(tmem + lane_off + Lay::kColDPT + c * 16, dsw);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&p_ready[c]);   // the products over these 32 queries may start
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(p_ready);      // dV += P^T dO_i and dK += dS^T Q_i may start
 
             // dS (row t = key t) into the MN-major, 128-byte-swizzled A operand
             // of dQ = dS K, once the staging of dQ_{i-1} has left the buffer;
