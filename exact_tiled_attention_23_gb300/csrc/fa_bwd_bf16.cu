@@ -192,15 +192,31 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             constexpr uint32_t id_acc = make_idesc(BK, D, 0, 1);    // dV, dK: A in TMEM, B MN-major
             constexpr uint32_t id_dq = make_idesc(BQ, D, 1, 1);     // dQ: A = dS MN-major, B = K MN-major
 
-            bool ok = wait_bounded(kv_full, 0, p.wait_limit_ns, kSiteQFull, ab);
+            auto issue_dpt = [&](int stage) {   // dP^T = V_j dO_i^T
+                const uint64_t dO_km = make_sdesc(base + Lay::kStageOff + stage * Lay::kStageBytes + Lay::kTileBytes,
+                                                  16, 1024);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t off = (uint64_t)(((k / 4) * Lay::kChunkBytes + (k % 4) * 32) >> 4);
+                    ptx::mma_ss(tmem + Lay::kColDPT, dV_km + off, dO_km + off, id_st, k > 0);
+                }
+            };
+            // dP^T of a query tile is issued right after dQ of the one before:
+            // its columns are free once dK has read dS^T and the key-row
+            // threads have copied dS out (ds_ready), while S^T waits for the
+            // dQ rows to leave TMEM.
+            bool ok = wait_bounded(kv_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
+                      wait_bounded(&stage_full[0], 0, p.wait_limit_ns, kSiteSlotFull, ab);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_dpt(0);
+            }
             for (int it = 0; it < n_iter && ok; ++it) {
                 const int s = it & 1;
                 const uint32_t st = base + Lay::kStageOff + s * Lay::kStageBytes;
                 const uint64_t dQ_km = make_sdesc(st, 16, 1024);
-                const uint64_t dO_km = make_sdesc(st + Lay::kTileBytes, 16, 1024);
                 const uint64_t dQ_mn = make_sdesc(st, Lay::kChunkBytes, 1024);
                 const uint64_t dO_mn = make_sdesc(st + Lay::kTileBytes, Lay::kChunkBytes, 1024);
-                if (!wait_bounded(&stage_full[s], (it >> 1) & 1, p.wait_limit_ns, kSiteSlotFull, ab)) break;
                 // dQ_{i-1} has left the S^T columns
                 if (it > 0 && !wait_bounded(dq_free, (it - 1) & 1, p.wait_limit_ns, kSitePFull, ab)) break;
                 ptx::tc_fence_after();
@@ -208,11 +224,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t off = (uint64_t)(((k / 4) * Lay::kChunkBytes + (k % 4) * 32) >> 4);
                     ptx::mma_ss(tmem + Lay::kColST, dK_km + off, dQ_km + off, id_st, k > 0);
-                }
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t off = (uint64_t)(((k / 4) * Lay::kChunkBytes + (k % 4) * 32) >> 4);
-                    ptx::mma_ss(tmem + Lay::kColDPT, dV_km + off, dO_km + off, id_st, k > 0);
                 }
                 ptx::mma_commit(s_full);
                 // dV += P^T dO_i and dK += dS^T Q_i, 32 queries (two K-steps)
@@ -241,7 +252,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     ptx::mma_ss(tmem + Lay::kColST, dS_mn + off, dK_mn + off, id_dq, k > 0);
                 }
                 ptx::mma_commit(dq_full);
-                if (it + 1 == n_iter) ptx::mma_commit(acc_full);
+                if (it + 1 == n_iter) {
+                    ptx::mma_commit(acc_full);
+                } else {
+                    const int s1 = (it + 1) & 1;
+                    if (!wait_bounded(&stage_full[s1], ((it + 1) >> 1) & 1, p.wait_limit_ns, kSiteSlotFull, ab)) break;
+                    ptx::tc_fence_after();
+                    issue_dpt(s1);
+                }
             }
             ptx::mma_commit(mma_drain);
             wait_bounded(mma_drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
