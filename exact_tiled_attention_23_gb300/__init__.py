@@ -239,7 +239,8 @@ def default_scale(D: int) -> float:
 def backward(q, k, v, o, do, lse, causal: bool = True, scale=None, kv_len=None, workspace=None,
              stream=None):
     """(dQ, dK, dV) of sum(O * dO) for O, LSE = forward(q, k, v, ...), bf16
-    CUDA tensors [B, H, N, D] (LSE fp32 [B, H, N]).  The workspace (a CUDA
+    CUDA tensors [B, H, N, D] with D a multiple of 8 up to 128 (LSE fp32
+    [B, H, N]).  The workspace (a CUDA
     tensor of at least fa_bwd_workspace_bytes bytes) is allocated here with
     torch when not given."""
     import torch

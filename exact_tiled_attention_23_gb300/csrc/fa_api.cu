@@ -50,8 +50,9 @@ uint64_t wait_limit_ns()
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Head dimensions of the split-capable tensor-core forward: multiples of 8
-// (a TMA row stride must be a multiple of 16 bytes) up to 128.
+// Head dimensions of the tensor-core kernels that zero-pad to 64 / 128 (the
+// forward, its split-KV form and the backward): multiples of 8 (a TMA row
+// stride must be a multiple of 16 bytes) up to 128.
 bool tc_fwd_head_dim(int D) { return D > 0 && D <= 128 && D % 8 == 0; }
 
 fa_status check_common(const void *Q, const void *K, const void *V, const void *O, int B, int H,
@@ -271,7 +272,7 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     if (st != FA_OK) return st;
     if ((int64_t)B * H * N == 0) return FA_OK;
     if (!O || !dO || !LSE || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!tc_fwd_head_dim(D)) return FA_ERR_UNSUPPORTED;
     const void *ptrs16[] = {Q, K, V, O, dO, dQ, dK, dV, workspace};
     for (const void *ptr : ptrs16)
         if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;

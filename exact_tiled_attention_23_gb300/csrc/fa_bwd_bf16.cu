@@ -380,15 +380,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             have = ptx::bar_and(1, 128, have && wait_bounded(acc_full, 0, p.wait_limit_ns, kSiteOFinal, ab));
         if (have || n_iter == 0) {
             ptx::tc_fence_after();
-            uint16_t *dk_row = static_cast<uint16_t *>(p.dk) + (bh * N + key) * D;
-            uint16_t *dv_row = static_cast<uint16_t *>(p.dv) + (bh * N + key) * D;
+            const int Dv = (int)p.D;                            // real columns (a multiple of 8, <= D)
+            uint16_t *dk_row = static_cast<uint16_t *>(p.dk) + (bh * N + key) * Dv;
+            uint16_t *dv_row = static_cast<uint16_t *>(p.dv) + (bh * N + key) * Dv;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = which ? Lay::kColDK : Lay::kColDV;
                 const float mul = which ? p.scale : 1.f;
                 uint16_t *dst_row = which ? dk_row : dv_row;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 32 && c * 32 < Dv; ++c) {
                     uint32_t v[32];
                     if (n_iter > 0) {
                         ptx::tmem_ld32(tmem + lane_off + col + c * 32, v);
@@ -401,7 +402,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                             w[e] = n_iter > 0 ? ptx::pack_bf16x2(u2f(v[2 * e]) * mul, u2f(v[2 * e + 1]) * mul) : 0u;
                         uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e)
+                            if (c * 32 + 8 * e < Dv)
+                                dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
                     }
                 }
             }
@@ -413,6 +416,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const int t = quarter * 32 + lane;                      // TMEM lane: query q0 + t
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         float *stage = reinterpret_cast<float *>(smem + Lay::kDSOff);
+        const int Dv = (int)p.D;                                // real columns (a multiple of 8, <= D)
         for (int it = 0; it < n_iter; ++it) {
             const int64_t q0 = (i0 + it) * BQ;
             if (!ptx::bar_and(2, 128, wait_bounded(dq_full, it & 1, p.wait_limit_ns, kSiteOFinal, ab))) break;
@@ -432,6 +436,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             ptx::mbar_arrive(dq_free);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
+                if (c * 32 >= Dv) break;                 // zero padding past the real columns
                 float *buf = stage + (c & 1) * (BQ * 32);
                 if (c >= 2) {
                     // the reduce that read this buffer two chunks ago is done
@@ -467,29 +472,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
 }
 
-// Delta = rowsum(dO * O) per query row, and the zeroed fp32 dQ accumulator.
-// One warp per row.
-template <int D>
+// Delta = rowsum(dO * O) per query row (over the D real columns), and the
+// zeroed fp32 dQ accumulator.  One warp per row.
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ d_o,
-                float *__restrict__ delta, float *__restrict__ dq_acc, int64_t rows)
+                float *__restrict__ delta, float *__restrict__ dq_acc, int64_t rows, int D)
 {
-    constexpr int kPer = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
     float s = 0.f;
-#pragma unroll
-    for (int c = 0; c < kPer; ++c) {
-        const int64_t idx = row * D + lane * kPer + c;
+    for (int c = lane; c < D; c += 32) {
+        const int64_t idx = row * D + c;
         s = fmaf(__uint_as_float((uint32_t)o[idx] << 16), __uint_as_float((uint32_t)d_o[idx] << 16), s);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0) delta[row] = s;
-    float *acc = dq_acc + row * D + lane * kPer;
-#pragma unroll
-    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+    for (int c = lane; c < D; c += 32) dq_acc[row * D + c] = 0.f;
 }
 
 // dQ = scale * accumulator, rounded to bf16 (two elements per thread).
@@ -516,15 +516,16 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
         configured = true;
     }
     const int64_t rows = p.B * p.H * p.N;
-    bwd_prep_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const uint16_t *>(p.o), static_cast<const uint16_t *>(p.d_o), p.delta, p.dq_acc, rows);
+    bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(p.o), static_cast<const uint16_t *>(p.d_o), p.delta, p.dq_acc, rows,
+        (int)p.D);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t ctas = p.B * p.H * ((p.N + BK - 1) / BK);
     bwd_kernel<D><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t n2 = rows * D / 2;
+    const int64_t n2 = rows * p.D / 2;
     bwd_dq_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t *>(p.dq),
                                                                   p.scale, n2);
     return cudaGetLastError();
@@ -536,9 +537,12 @@ cudaError_t launch_bwd_bf16(const BwdParams &p, const CUtensorMap &tm_q, const C
                             const CUtensorMap &tm_v, const CUtensorMap &tm_do, const CUtensorMap &tm_dq,
                             cudaStream_t stream)
 {
-    if (p.D == 64) return launch_bwd_d<64>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
-    if (p.D == 128) return launch_bwd_d<128>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
-    return cudaErrorInvalidValue;
+    // D a multiple of 8 below 128 runs at the next of 64 / 128: the TMA boxes
+    // fill the columns past D with zeros, which adds nothing to any product,
+    // and only the D real columns of dQ, dK and dV are written.
+    if (p.D % 8 != 0 || p.D <= 0 || p.D > 128) return cudaErrorInvalidValue;
+    if (p.D <= 64) return launch_bwd_d<64>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
+    return launch_bwd_d<128>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
 }
 
 cudaError_t read_and_clear_status_bwd(uint32_t *out)

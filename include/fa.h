@@ -199,7 +199,9 @@ fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, vo
  *   LSE             const float [B,H,N]: the LSE fa_fwd returned.
  *   dQ, dK, dV      bf16 [B,H,N,D] outputs (fp32 accumulation, rounded to
  *                   nearest even); keys at or past kv_len get zero dK, dV.
- *   B,H,N,D, causal, scale, kv_len: as in the forward call; D in {64, 128}.
+ *   B,H,N,D, causal, scale, kv_len: as in the forward call; D a multiple
+ *            of 8 up to 128 (zero-padded to 64 / 128 like the forward; 256
+ *            gives FA_ERR_UNSUPPORTED).
  *   workspace       caller-owned device memory, 16-byte aligned, of at least
  *                   fa_bwd_workspace_bytes(B,H,N,D) bytes (an fp32 dQ
  *                   accumulator and Delta); fully rewritten by each call;

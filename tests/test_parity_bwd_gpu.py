@@ -65,6 +65,11 @@ CASES = [
     (1, 1, 128, 64, True, None),
     (1, 2, 256, 128, False, None),
     (2, 2, 300, 64, True, [300, 0]),
+    # head dims below 128 run zero-padded to 64 / 128
+    (1, 2, 200, 32, True, None),
+    (2, 1, 300, 96, False, [300, 77]),
+    (1, 1, 257, 40, True, None),
+    (1, 1, 130, 8, False, None),
     (1, 2, 640, 128, True, [500]),
     (2, 1, 777, 128, False, [777, 129]),
     (1, 2, 1024, 64, True, None),
@@ -75,3 +80,33 @@ CASES = [
 def test_bwd_matches_oracle(B, H, N, D, causal, kv_len):
     stats = run_case(B, H, N, D, causal, kv_len, seed=N + D)
     print(stats)
+
+
+@pytest.mark.parametrize("D", [40, 96])
+def test_bwd_head_dim_writes_stay_in_bounds(D):
+    """dQ, dK and dV go to views of larger buffers: nothing past the last
+    row's D columns changes (the zero-padded columns are never stored)."""
+    B, H, N = 1, 2, 300
+    inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=True, seed=D + 5)
+    g = torch.Generator("cpu").manual_seed(D)
+    do = torch.randn((B, H, N, D), generator=g).to(torch.bfloat16).cuda()
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    o, lse = fa.forward(q, k, v, causal=True)
+    n = B * H * N * D
+    bufs = [torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, H, N, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                   bufs[0].data_ptr(), bufs[1].data_ptr(), bufs[2].data_ptr(), B, H, N, D, True,
+                   float("nan"), None, ws.data_ptr(), ws_bytes, None)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    for buf in bufs:
+        assert torch.all(buf[n:] == 7.0)
+    # the same gradients as the allocating entry point
+    dq, dk, dv = fa.backward(q, k, v, o, do, lse, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(bufs[1][:n].view(B, H, N, D), dk)
+    assert torch.equal(bufs[2][:n].view(B, H, N, D), dv)
+    assert (bufs[0][:n].view(B, H, N, D).float() - dq.float()).abs().max().item() <= 1e-2 * dq.float().abs().max().item()
