@@ -75,8 +75,8 @@ KERNEL_SOURCES = {
                         "fa_internal.h", "fa_api.cu"),
     "bwd_kernel": ("fa_bwd_bf16.cu", "fa_tc_common.cuh", "sm103_ptx.cuh", "fa_internal.h", "fa_api.cu"),
     "fwd_fp32_kernel": ("fa_fwd_fp32.cu", "fa_internal.h", "fa_api.cu"),
-    "fwd_d256_kernel": ("fa_fwd_d256.cu", "fa_fwd_softmax.cuh", "fa_tc_common.cuh", "sm103_ptx.cuh",
-                        "fa_internal.h", "fa_api.cu"),
+    "fwd_onetile_kernel": ("fa_fwd_onetile.cu", "fa_fwd_softmax.cuh", "fa_tc_common.cuh", "sm103_ptx.cuh",
+                           "fa_internal.h", "fa_api.cu"),
 }
 
 
@@ -366,7 +366,14 @@ def run_ours(args, rank, world, local):
     if w.dtype in ("bf16", "fp16"):
         # fp16 and bf16 have the same dense tensor rate (kind::f16)
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
-        kname = "bwd_kernel" if args.pass_ == "bwd" else "fwd_d256_kernel" if D == 256 else "fwd_bf16_kernel"
+        # the library runs one 128-row query tile per CTA for D = 256 and for
+        # grids whose one-tile CTAs fit in one wave (FA_FWD_TILES forces it)
+        items = B * H * ((N + 255) // 256)
+        forced = os.environ.get("FA_FWD_TILES", "")
+        one_tile = D == 256 or forced == "1" or (
+            forced != "2" and 2 * items <= torch.cuda.get_device_properties(dev).multi_processor_count)
+        kname = ("bwd_kernel" if args.pass_ == "bwd" else
+                 "fwd_onetile_kernel" if splits is None and one_tile else "fwd_bf16_kernel")
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name, kname),
                     "peak_kind": f"{peak_kind} dense bf16 (burst)",

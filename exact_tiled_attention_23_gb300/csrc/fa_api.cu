@@ -50,6 +50,28 @@ uint64_t wait_limit_ns()
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Query tiles per CTA of the tensor-core forward that FA_FWD_TILES asks for:
+// "1" or "2", else 0 (the automatic choice).  Read on every call, so that a
+// process can compare the two kernels.
+int forced_tiles()
+{
+    const char *e = std::getenv("FA_FWD_TILES");
+    if (!e) return 0;
+    if (e[0] == '1' && e[1] == 0) return 1;
+    if (e[0] == '2' && e[1] == 0) return 2;
+    return 0;
+}
+
+// SMs of the current device (148 if it cannot be read).
+int sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
+    return sms;
+}
+
 // Head dimensions of the tensor-core kernels that zero-pad to 64 / 128 (the
 // forward, its split-KV form and the backward): multiples of 8 (a TMA row
 // stride must be a multiple of 16 bytes) up to 128.
@@ -148,11 +170,15 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
     if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
     if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
-    // one work item covers 256 query rows of one head (128 for D = 256); the
-    // grid is 1-D
-    const int64_t rows_per_item = D == 256 ? 128 : 256;
-    const int64_t items = (int64_t)B * H * (((int64_t)N + rows_per_item - 1) / rows_per_item);
-    if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
+    // The two-tile kernel's work item covers 256 query rows of one head; the
+    // one-tile kernel's covers 128 and runs D = 256, and grids whose twice as
+    // many one-tile CTAs still fit in one wave (one CTA per SM).  The grid is
+    // 1-D.
+    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    const int forced = forced_tiles();
+    const bool one_tile = D == 256 || forced == 1 || (forced == 0 && 2 * items <= sm_count());
+    const int64_t ctas = one_tile ? (int64_t)B * H * (((int64_t)N + 127) / 128) : items;
+    if (ctas > INT32_MAX) return FA_ERR_INVALID_ARG;
     const int64_t BH = (int64_t)B * H;
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tq, tk, tv;
@@ -161,7 +187,7 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
         return FA_ERR_CUDA;
     fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
     p.f16 = f16 ? 1 : 0;
-    cudaError_t e = D == 256 ? fa::launch_fwd_d256(p, tq, tk, tv, static_cast<cudaStream_t>(stream))
+    cudaError_t e = one_tile ? fa::launch_fwd_onetile(p, tq, tk, tv, static_cast<cudaStream_t>(stream))
                              : fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -193,10 +219,7 @@ int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D)
 {
     (void)D;
     if (B <= 0 || H <= 0 || N <= 0) return 1;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        sms = 148;
+    const int sms = sm_count();
     // one CTA per SM (shared memory), so fill one wave without a ragged second
     // one, and keep at least two key blocks in every range
     const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
@@ -329,7 +352,7 @@ fa_status fa_device_status(void *stream)
 {
     uint32_t v = 0, vb = 0, vd = 0;
     if (fa::read_and_clear_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess ||
-        fa::read_and_clear_status_bwd(&vb) != cudaSuccess || fa::read_and_clear_status_d256(&vd) != cudaSuccess)
+        fa::read_and_clear_status_bwd(&vb) != cudaSuccess || fa::read_and_clear_status_onetile(&vd) != cudaSuccess)
         return FA_ERR_CUDA;
     v |= vb | vd;
     if (v) {

@@ -1,18 +1,19 @@
-// fa_fwd_d256.cu -- bf16 / fp16 attention forward on the tensor cores for
-// head dimension 256.
+// fa_fwd_onetile.cu -- bf16 / fp16 attention forward on the tensor cores with
+// one 128-row query tile per CTA.
 //
 // The computation is the tiled online-softmax forward of "vectorized-flash-
 // attention-kernel" (Core algorithm; Key design decisions 1-3), with the same
-// per-row softmax step as the D <= 128 kernel (fa_fwd_softmax.cuh).  Only the
-// layout on the SM differs, because a D = 256 output tile takes 256 of the 512
-// TMEM columns:
+// per-row softmax step as the two-tile kernel (fa_fwd_softmax.cuh).  Only the
+// layout on the SM differs.  It serves head dimension 256, whose output tile
+// takes 256 of the 512 TMEM columns, and grids where the two-tile kernel's
+// 256-row items would not fill the GPU (twice as many CTAs):
 //
 //   * one CTA owns one 128-row query tile; TMEM holds two score tiles S_a,
-//     S_b (128 columns each) and O (256 columns);
+//     S_b (128 columns each) and O (D columns);
 //   * warp 1 issues S_{j+1} = Q K_{j+1}^T into the other score tile before
 //     O += P_j V_j, so the tensor core computes the next block's scores while
 //     warps 4-7 run the softmax of this one;
-//   * shared memory holds Q (64 KB) and one K and one V tile (64 KB each);
+//   * shared memory holds Q and one K and one V tile (D x 256 bytes each);
 //     warp 0 loads K_{j+1} as soon as S_j has consumed K_j, ahead of V_j,
 //     which waits for O += P_{j-1} V_{j-1}.
 //
@@ -32,38 +33,47 @@
 
 namespace fa {
 
-__device__ uint32_t g_status_d256;
+__device__ uint32_t g_status_onetile;
 
 namespace {
 
-constexpr int D = 256;
 constexpr int BM = 128;                         // query rows per CTA (= TMEM lanes)
 constexpr int BN = 128;                         // keys per block
 constexpr int kThreads = 256;                   // warp 0 TMA, warp 1 MMA, warps 4-7 softmax
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms per row
 constexpr int kChunkBytes = 128 * 128;          // one 128-row x 64-column 16-bit box
-constexpr int kTileBytes = kChunks * kChunkBytes;   // 64 KB: Q, a K or a V tile
-constexpr int kQOff = 0;
-constexpr int kKOff = kTileBytes;
-constexpr int kVOff = 2 * kTileBytes;
-constexpr int kBarOff = 3 * kTileBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;    // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;                     // S_a [0,128), S_b [128,256), O [256,512)
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kColO = 256;                 // S_a [0,128), S_b [128,256), O [256,256+D)
+
+template <int D>
+struct OneTileLayout {
+    static constexpr int kChunks = D / 64;                  // 128-byte swizzle atoms per row
+    static constexpr int kTileBytes = kChunks * kChunkBytes;    // Q, a K or a V tile
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kTileBytes;
+    static constexpr int kVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = 3 * kTileBytes;
+    // At least 120 KB, so that one CTA (and its 512 TMEM columns) sits on an SM.
+    static constexpr int kNeed = kBarOff + 256 + 1024;      // + alignment slack
+    static constexpr int kSmemBytes = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
+    static_assert(D == 64 || D == 128 || D == 256, "head dim");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 __device__ __forceinline__ uint32_t col_s(int buf) { return (uint32_t)buf * 128u; }
 
-template <bool kF16>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
-fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int q_tiles)
 {
+    using Lay = OneTileLayout<D>;
+    constexpr int kChunks = Lay::kChunks, kTileBytes = Lay::kTileBytes;
+    constexpr int kQOff = Lay::kQOff, kKOff = Lay::kKOff, kVOff = Lay::kVOff;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
     uint64_t *q_full = bars + 0;
     uint64_t *k_full = bars + 1;
     uint64_t *k_empty = bars + 2;
@@ -76,7 +86,7 @@ fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t *mma_drain = bars + 11;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
-    const Abort ab{abort_word, &g_status_d256};
+    const Abort ab{abort_word, &g_status_onetile};
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -260,10 +270,13 @@ fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const bool empty = !(st.l > 0.f);
             const float inv = empty ? 0.f : 1.f / st.l;
             const float lse_row = empty ? -INFINITY : (st.m_ref + log2f(st.l)) * 0.69314718055994530942f;
+            // Only the first p.D (a multiple of 8, <= D) columns exist in
+            // memory; the rest of the D computed ones are the zero padding.
+            const int Dv = (int)p.D;
             const int64_t flat = bh * N + row;
-            uint16_t *orow = static_cast<uint16_t *>(p.o) + flat * D;
+            uint16_t *orow = static_cast<uint16_t *>(p.o) + flat * Dv;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 32 && c * 32 < Dv; ++c) {
                 uint32_t o[32];
                 if (n_kv > 0) {
                     ptx::tmem_ld32(tO + c * 32, o);
@@ -280,7 +293,9 @@ fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                    for (int t = 0; t < 4; ++t)
+                        if (c * 32 + 8 * t < Dv)
+                            dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                 }
             }
             if (row < N && p.lse) p.lse[flat] = lse_row;
@@ -295,40 +310,52 @@ fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <bool kF16>
+template <int D, bool kF16>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                    cudaStream_t stream)
 {
+    using Lay = OneTileLayout<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_d256_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(fwd_onetile_kernel<D, kF16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int q_tiles = (int)((p.N + BM - 1) / BM);
     const int64_t ctas = p.B * p.H * (int64_t)q_tiles;
-    fwd_d256_kernel<kF16><<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p, q_tiles);
+    fwd_onetile_kernel<D, kF16><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_tiles);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_f(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                     cudaStream_t stream)
+{
+    return p.f16 ? launch<D, true>(p, tq, tk, tv, stream) : launch<D, false>(p, tq, tk, tv, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_d256(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                            const CUtensorMap &tm_v, cudaStream_t stream)
+// D = 256, or a multiple of 8 up to 128 run at the next of 64 / 128 with
+// zero-filled columns (as in the two-tile kernel).
+cudaError_t launch_fwd_onetile(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                               const CUtensorMap &tm_v, cudaStream_t stream)
 {
-    if (p.D != D) return cudaErrorInvalidValue;
-    return p.f16 ? launch<true>(p, tm_q, tm_k, tm_v, stream) : launch<false>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 256) return launch_f<256>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D % 8 != 0 || p.D <= 0 || p.D > 128) return cudaErrorInvalidValue;
+    if (p.D <= 64) return launch_f<64>(p, tm_q, tm_k, tm_v, stream);
+    return launch_f<128>(p, tm_q, tm_k, tm_v, stream);
 }
 
-cudaError_t read_and_clear_status_d256(uint32_t *out)
+cudaError_t read_and_clear_status_onetile(uint32_t *out)
 {
     uint32_t v = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_d256, sizeof(v));
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_onetile, sizeof(v));
     if (e != cudaSuccess) return e;
     if (v) {
         const uint32_t zero = 0;
-        e = cudaMemcpyToSymbol(g_status_d256, &zero, sizeof(zero));
+        e = cudaMemcpyToSymbol(g_status_onetile, &zero, sizeof(zero));
         if (e != cudaSuccess) return e;
     }
     *out = v;

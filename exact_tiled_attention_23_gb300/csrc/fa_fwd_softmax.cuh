@@ -46,15 +46,19 @@ struct OnlineRow {
     __device__ __forceinline__ void raise(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tO,
                                           Hook &before_o_touch)
     {
+        // Eight running maxima: scores 0..7, then 16 per step over 8..119
+        // (two per 3-input max), then 120..127.
         float mx8[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx8[a] = u2f(s[0][a]);
 #pragma unroll
-        for (int k = 8; k < 128; k += 16)
+        for (int k = 8; k < 120; k += 16)
 #pragma unroll
             for (int a = 0; a < 8; ++a)
                 mx8[a] = ptx::max3(mx8[a], u2f(s[(k + 2 * a) / 32][(k + 2 * a) % 32]),
                                    u2f(s[(k + 2 * a + 1) / 32][(k + 2 * a + 1) % 32]));
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(mx8[a], u2f(s[3][24 + a]));
         const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
                                fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_ref, mx * sl2);

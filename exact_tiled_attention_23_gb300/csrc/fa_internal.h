@@ -68,8 +68,9 @@ cudaError_t launch_fwd_fp32(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, cudaStream_t stream);
 
-// Head dimension 256 (one 128-row query tile per CTA).
-cudaError_t launch_fwd_d256(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+// One 128-row query tile per CTA: head dimension 256, and grids too small for
+// the two-tile kernel to fill the GPU.
+cudaError_t launch_fwd_onetile(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, cudaStream_t stream);
 
 // Split-KV forward: partial kernel over key-block ranges, then the merge.
@@ -85,7 +86,7 @@ cudaError_t launch_bwd_bf16(const BwdParams &p, const CUtensorMap &tm_q, const C
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out);
 // The backward kernels' status word (call after read_and_clear_status).
 cudaError_t read_and_clear_status_bwd(uint32_t *out);
-// The D = 256 forward kernel's status word (call after read_and_clear_status).
-cudaError_t read_and_clear_status_d256(uint32_t *out);
+// The one-tile forward kernel's status word (call after read_and_clear_status).
+cudaError_t read_and_clear_status_onetile(uint32_t *out);
 
 }  // namespace fa

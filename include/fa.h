@@ -70,13 +70,19 @@ typedef enum fa_status {
  *            FA_ERR_UNSUPPORTED.  Below 128 the tensor cores run at D
  *            rounded up to 64 or 128 with zero-filled columns, which leave
  *            every score unchanged; only the D real columns of O are
- *            written.  D = 256 has a kernel of its own (one 128-row query
- *            tile per CTA).
+ *            written.
  *   causal   nonzero: key j is hidden from query i when j > i.
  *   scale    softmax scale; NaN or <= 0 selects the default 1/sqrt(D)
  *            ("vectorized-flash-attention-kernel", Constructor options).
  *   kv_len   const int32 [B] device pointer of key lengths, or NULL (= N).
  *   stream   cudaStream_t to enqueue on.
+ *
+ * Two kernels serve this call.  One gives every CTA two 128-row query tiles
+ * (D <= 128); the other gives it one (any D here), for D = 256 and for grids
+ * whose one-tile CTAs (2 * B * H * ceil(N/256)) fit in one wave of the GPU's
+ * SMs.  The
+ * environment variable FA_FWD_TILES = "1" or "2", read on every call, forces
+ * one of them (D = 256 always runs the one-tile kernel).
  *
  * Accumulation is fp32 (scores, running sums, O); P is rounded to bf16 for
  * the second product.  Returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED from

@@ -26,6 +26,14 @@ BF16_MAX, BF16_MEAN = 2e-2, 2e-3
 FP32_MAX = 1e-5
 
 
+@pytest.fixture(params=["1", "2"], ids=["one_tile", "two_tile"])
+def tiles(request, monkeypatch):
+    """Run a test under each tensor-core forward kernel: one or two 128-row
+    query tiles per CTA (the library reads FA_FWD_TILES on every call)."""
+    monkeypatch.setenv("FA_FWD_TILES", request.param)
+    return request.param
+
+
 @pytest.fixture(scope="module", autouse=True)
 def built():
     fa.build()
@@ -110,21 +118,21 @@ BF16_CASES = [
 
 
 @pytest.mark.parametrize("B,H,N,D,causal,kv_len", BF16_CASES)
-def test_bf16_small_cases(B, H, N, D, causal, kv_len):
+def test_bf16_small_cases(B, H, N, D, causal, kv_len, tiles):
     inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=causal, seed=N + D, kv_len=kv_len)
     o, lse = run_gpu(inp)
     compare(inp, o, lse)
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_bf16_explicit_scale(D):
+def test_bf16_explicit_scale(D, tiles):
     inp = workloads.make_case(2, 2, 384, D, dtype="bf16", causal=True, seed=7)
     o, lse = run_gpu(inp, scale=0.3)
     compare(inp, o, lse, scale=0.3)
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_bf16_large_logits(D):
+def test_bf16_large_logits(D, tiles):
     """Query rows scaled x30 and x-30: the running max jumps between key
     blocks, so the O rescale path runs; results stay exact within tolerance."""
     inp = workloads.make_case(1, 2, 768, D, dtype="bf16", causal=True, seed=11)
@@ -138,7 +146,7 @@ def test_bf16_large_logits(D):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [True, False])
-def test_bf16_growing_logits(D, causal):
+def test_bf16_growing_logits(D, causal, tiles):
     """Key magnitudes ramp x1 -> x60 along the sequence and some query rows
     are scaled x3: later key blocks keep raising the row max far above the
     reference taken from earlier blocks, so the rescale path runs on many
@@ -203,7 +211,7 @@ F16_CASES = [
 
 
 @pytest.mark.parametrize("B,H,N,D,causal,kv_len", F16_CASES)
-def test_f16_small_cases(B, H, N, D, causal, kv_len):
+def test_f16_small_cases(B, H, N, D, causal, kv_len, tiles):
     """fp16 operands: the same kernel with f16 MMA operands and an fp16 P."""
     inp = workloads.make_case(B, H, N, D, dtype="fp16", causal=causal, seed=N + 5 * D, kv_len=kv_len)
     o, lse = run_gpu(inp)
@@ -211,7 +219,7 @@ def test_f16_small_cases(B, H, N, D, causal, kv_len):
     compare(inp, o, lse)
 
 
-def test_f16_large_logits():
+def test_f16_large_logits(tiles):
     """x30 query rows: the fp16 lazy limit (block sum 2^15) forces frequent
     reference moves; P stays inside the fp16 range."""
     inp = workloads.make_case(1, 2, 1024, 128, dtype="fp16", causal=True, seed=17)
@@ -243,14 +251,14 @@ HEAD_DIM_CASES = [
 
 
 @pytest.mark.parametrize("B,H,N,D,dtype,causal,kv_len", HEAD_DIM_CASES)
-def test_head_dims(B, H, N, D, dtype, causal, kv_len):
+def test_head_dims(B, H, N, D, dtype, causal, kv_len, tiles):
     inp = workloads.make_case(B, H, N, D, dtype=dtype, causal=causal, seed=N + 3 * D, kv_len=kv_len)
     o, lse = run_gpu(inp)
     compare(inp, o, lse)
 
 
 @pytest.mark.parametrize("D", [32, 96, 256])
-def test_head_dim_writes_stay_in_bounds(D):
+def test_head_dim_writes_stay_in_bounds(D, tiles):
     """O is written through a view of a larger buffer: nothing past the last
     row's D columns changes (the padded columns are never stored)."""
     B, H, N = 1, 2, 300
@@ -315,7 +323,20 @@ def test_fp32_small_cases(B, H, N, D, causal, kv_len):
     compare(inp, o, lse)
 
 
-def test_outputs_are_deterministic():
+@pytest.mark.parametrize("D", [64, 128])
+def test_one_and_two_tile_kernels_agree(D, monkeypatch):
+    """The two forward kernels run the same per-row steps in the same key
+    order; their outputs agree to the last bf16 rounding step."""
+    inp = workloads.make_case(2, 3, 700, D, dtype="bf16", causal=True, seed=D + 1, kv_len=[700, 333])
+    monkeypatch.setenv("FA_FWD_TILES", "1")
+    o1, l1 = run_gpu(inp)
+    monkeypatch.setenv("FA_FWD_TILES", "2")
+    o2, l2 = run_gpu(inp)
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+    assert torch.allclose(l1, l2, rtol=0, atol=1e-4)
+
+
+def test_outputs_are_deterministic(tiles):
     inp = workloads.make_case(2, 4, 777, 128, dtype="bf16", causal=True, seed=3, kv_len=[777, 400])
     o1, l1 = run_gpu(inp)
     o2, l2 = run_gpu(inp)
