@@ -24,6 +24,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "
            "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "FA_MAX_SPLITS",
            "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES", "fa_fwd_f16",
            "fa_bwd", "fa_bwd_workspace_bytes", "backward",
+           "fa_fwd_from_host", "fa_fwd_from_host_auto_groups", "FA_MAX_HOST_GROUPS", "forward_from_host",
            "forward", "build"]
 
 FA_OK = 0
@@ -33,6 +34,7 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_MAX_SPLITS = 64
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
+FA_MAX_HOST_GROUPS = 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +95,10 @@ def load():
         lib.fa_bwd.restype = i32
         lib.fa_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_from_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, f32, vp, i32, i32, vp]
+        lib.fa_fwd_from_host.restype = i32
+        lib.fa_fwd_from_host_auto_groups.argtypes = [i32, i32, i32, i32]
+        lib.fa_fwd_from_host_auto_groups.restype = i32
         _lib = lib
         return lib
 
@@ -139,6 +145,19 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, causal, scale, kv_len, w
     """bf16 backward by recomputation; pointers are device addresses or None."""
     return int(load().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, int(bool(causal)),
                              float(scale), kv_len, workspace, int(workspace_bytes), stream))
+
+
+def fa_fwd_from_host(Q_host, K_host, V_host, O_host, LSE_host, Q_dev, K_dev, V_dev, O_dev, LSE_dev,
+                     B, H, N, D, causal, scale, kv_len, f16, groups, stream) -> int:
+    """Forward over host arrays, copies overlapped with the computation in
+    `groups` (batch, head) groups; the device buffers are the caller's."""
+    return int(load().fa_fwd_from_host(Q_host, K_host, V_host, O_host, LSE_host, Q_dev, K_dev, V_dev,
+                                       O_dev, LSE_dev, B, H, N, D, int(bool(causal)), float(scale),
+                                       kv_len, int(bool(f16)), int(groups), stream))
+
+
+def fa_fwd_from_host_auto_groups(B, H, N, D) -> int:
+    return int(load().fa_fwd_from_host_auto_groups(B, H, N, D))
 
 
 def fa_bwd_workspace_bytes(B, H, N, D) -> int:
@@ -234,6 +253,57 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
 
 def default_scale(D: int) -> float:
     return 1.0 / math.sqrt(D)
+
+
+def forward_from_host(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse=None,
+                      device_buffers=None, groups: int = 0, stream=None):
+    """O, LSE = attention(q, k, v) for bf16 / fp16 CPU tensors [B, H, N, D]
+    (page-locked for asynchronous copies), through fa_fwd_from_host.  out
+    and lse are CPU tensors to write (allocated page-locked when None);
+    device_buffers = (q, k, v, o, lse) CUDA tensors of the same shapes
+    (allocated with torch when None).  kv_len: optional int32 CUDA tensor
+    [B].  Returns (out, lse) after the stream has finished."""
+    import torch
+
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all have shape [B, H, N, D]")
+    if q.is_cuda or k.is_cuda or v.is_cuda:
+        raise ValueError("q, k, v must be CPU tensors")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must share dtype bfloat16 or float16")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    if device_buffers is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        device_buffers = (torch.empty(q.shape, dtype=q.dtype, device=dev),
+                          torch.empty(q.shape, dtype=q.dtype, device=dev),
+                          torch.empty(q.shape, dtype=q.dtype, device=dev),
+                          torch.empty(q.shape, dtype=q.dtype, device=dev),
+                          torch.empty((B, H, N), dtype=torch.float32, device=dev))
+    qd, kd, vd, od, ld = device_buffers
+    kv_ptr = None
+    if kv_len is not None:
+        if kv_len.dtype != torch.int32 or not kv_len.is_cuda or kv_len.numel() != B:
+            raise ValueError("kv_len must be an int32 CUDA tensor with B entries")
+        kv_ptr = kv_len.contiguous().data_ptr()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    st = fa_fwd_from_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
+                          B, H, N, D, causal, float("nan") if scale is None else float(scale), kv_ptr,
+                          q.dtype == torch.float16, groups, sp)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_from_host")
+    if hasattr(stream, "synchronize"):
+        stream.synchronize()
+    else:
+        torch.cuda.synchronize()
+    return out, lse
 
 
 def backward(q, k, v, o, do, lse, causal: bool = True, scale=None, kv_len=None, workspace=None,

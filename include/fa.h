@@ -190,6 +190,54 @@ fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, vo
                                  const int32_t *kv_len, int num_splits, void *stream);
 
 /*
+ * fa_fwd_from_host -- fa_fwd (or fa_fwd_f16) over inputs and outputs in host
+ * memory, with the host<->device copies overlapped with the computation.  The
+ * paper has no counterpart: this is a library service for callers whose data
+ * starts and ends on the host.
+ *
+ * The (batch, head) slices are split into `groups` groups, none spanning two
+ * batches.  Group c is copied to the device on a library-owned copy stream.
+ * It is then computed on `stream` while group c+1 is copied in, and copied
+ * back on a second copy stream while group c+1 is computed.  On a
+ * Grace-Blackwell node the copies of a long-context problem take longer than
+ * the attention, so the overlap shortens the whole call.
+ *
+ *   Q_host, K_host, V_host  const [B,H,N,D] host arrays (bf16, or fp16 if f16
+ *                           is nonzero).  Page-locked memory lets the copies
+ *                           run asynchronously.
+ *   O_host                  [B,H,N,D] host array for O.
+ *   LSE_host                float [B,H,N] host array, or NULL to skip LSE.
+ *   Q_dev, K_dev, V_dev, O_dev  caller-owned device buffers of the same
+ *                           shape, 16-byte aligned.  The inputs are copied
+ *                           into them, and O is computed there.
+ *   LSE_dev                 float [B,H,N] device buffer; required when
+ *                           LSE_host is given, else may be NULL.
+ *   B,H,N,D, causal, scale, kv_len  as in fa_fwd (kv_len in device memory).
+ *   groups                  1..FA_MAX_HOST_GROUPS, or 0 for
+ *                           fa_fwd_from_host_auto_groups(B,H,N,D).
+ *   stream                  the caller's stream.  The copies start after the
+ *                           work already enqueued on it.  Work enqueued on it
+ *                           afterwards starts only once O and LSE are back in
+ *                           host memory.
+ *
+ * Returns as fa_fwd; all argument checks run before any CUDA call.  The first
+ * call on a device creates that device's two copy streams and their events.
+ * Calls on one device share them, so calls from different host threads are
+ * serialised on the copy engines.
+ */
+#define FA_MAX_HOST_GROUPS 1024
+
+fa_status fa_fwd_from_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
+                           float *LSE_host, void *Q_dev, void *K_dev, void *V_dev, void *O_dev,
+                           float *LSE_dev, int B, int H, int N, int D, int causal, float scale,
+                           const int32_t *kv_len, int f16, int groups, void *stream);
+
+/* The group count fa_fwd_from_host uses for groups = 0 on the current
+ * device: every group keeps at least three waves of 256-row work items
+ * (1 for empty problems). */
+int fa_fwd_from_host_auto_groups(int B, int H, int N, int D);
+
+/*
  * fa_bwd -- backward pass of fa_fwd by recomputation ("FlashAttention"
  * module F08, Math: backward via recomputation and the identity
  * rowsum(dP*P) = rowsum(dO*O); "vectorized-flash-attention-kernel", Key

@@ -131,3 +131,25 @@ def test_bwd_workspace_and_argument_checks(lib):
     assert fa.fa_bwd(P, P, P, P, P, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, P, need - 1, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd(P, P, P, P, P + 8, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, P, big, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd(None, None, None, None, None, None, None, None, None, 1, 1, 0, 64, 1, NAN, None, None, 0, None) == fa.FA_OK
+
+
+def test_from_host_argument_checks(lib):
+    """fa_fwd_from_host rejects bad arguments before creating streams or
+    copying anything."""
+    H_ = P + (1 << 20)      # stands in for a host array (never dereferenced here)
+    args = lambda **kw: dict(dict(Qh=H_, Kh=H_, Vh=H_, Oh=H_, Lh=None, Qd=P, Kd=P, Vd=P, Od=P, Ld=None,
+                                  B=1, H=2, N=16, D=64, groups=0), **kw)
+
+    def call(a):
+        return fa.fa_fwd_from_host(a["Qh"], a["Kh"], a["Vh"], a["Oh"], a["Lh"], a["Qd"], a["Kd"], a["Vd"],
+                                   a["Od"], a["Ld"], a["B"], a["H"], a["N"], a["D"], 1, NAN, None, 0,
+                                   a["groups"], None)
+    assert call(args(Qh=None)) == fa.FA_ERR_INVALID_ARG
+    assert call(args(Od=None)) == fa.FA_ERR_INVALID_ARG
+    assert call(args(Lh=H_, Ld=None)) == fa.FA_ERR_INVALID_ARG          # LSE wanted, no device buffer
+    assert call(args(groups=-1)) == fa.FA_ERR_INVALID_ARG
+    assert call(args(groups=fa.FA_MAX_HOST_GROUPS + 1)) == fa.FA_ERR_INVALID_ARG
+    assert call(args(D=100)) == fa.FA_ERR_UNSUPPORTED
+    assert call(args(Qd=P + 8)) == fa.FA_ERR_INVALID_ARG
+    assert call(args(B=-1)) == fa.FA_ERR_INVALID_ARG
+    assert call(args(N=0, Qh=None, Qd=None)) == fa.FA_OK                 # empty problem: nothing to do

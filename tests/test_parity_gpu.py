@@ -336,6 +336,40 @@ def test_one_and_two_tile_kernels_agree(D, monkeypatch):
     assert torch.allclose(l1, l2, rtol=0, atol=1e-4)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("groups", [0, 1, 3, 8])
+def test_from_host_matches_device_forward(dtype, groups):
+    """fa_fwd_from_host (copies overlapped with the computation, per group
+    of heads) gives exactly the device forward's O and LSE."""
+    inp = workloads.make_case(3, 3, 300, 64, dtype=dtype, causal=True, seed=groups + 9,
+                              kv_len=[300, 0, 123])
+    kv = inp.kv_len.cuda()
+    o_ref, l_ref = fa.forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), causal=True, kv_len=kv)
+    torch.cuda.synchronize()
+    qh, kh, vh = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+    o, lse = fa.forward_from_host(qh, kh, vh, causal=True, kv_len=kv, groups=groups)
+    assert fa.fa_device_status(None) == fa.FA_OK
+    assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, l_ref.cpu())
+    compare(inp, o_ref, l_ref)
+
+
+def test_from_host_without_lse_and_on_a_side_stream():
+    inp = workloads.make_case(1, 4, 513, 128, dtype="bf16", causal=False, seed=21)
+    o_ref, _ = fa.forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), causal=False)
+    torch.cuda.synchronize()
+    qh, kh, vh = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+    oh = torch.empty(qh.shape, dtype=qh.dtype, pin_memory=True)
+    dev = [torch.empty_like(o_ref) for _ in range(4)]
+    s = torch.cuda.Stream()
+    st = fa.fa_fwd_from_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(), None,
+                             dev[0].data_ptr(), dev[1].data_ptr(), dev[2].data_ptr(), dev[3].data_ptr(), None,
+                             1, 4, 513, 128, False, float("nan"), None, False, 2, s.cuda_stream)
+    assert st == fa.FA_OK
+    s.synchronize()
+    assert fa.fa_device_status(None) == fa.FA_OK
+    assert torch.equal(oh, o_ref.cpu())
+
+
 def test_outputs_are_deterministic(tiles):
     inp = workloads.make_case(2, 4, 777, 128, dtype="bf16", causal=True, seed=3, kv_len=[777, 400])
     o1, l1 = run_gpu(inp)
