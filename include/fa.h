@@ -196,9 +196,10 @@ fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, vo
  * starts and ends on the host.
  *
  * The (batch, head) slices are split into `groups` groups, none spanning two
- * batches.  Group c is copied to the device on a library-owned copy stream.
- * It is then computed on `stream` while group c+1 is copied in, and copied
- * back on a second copy stream while group c+1 is computed.  On a
+ * batches.  Group c is copied to the device on a library-owned copy stream,
+ * computed on one of two library-owned compute streams (alternating, so that
+ * consecutive groups' kernels can share the SMs) while group c+1 is copied
+ * in, and copied back on a second copy stream.  On a
  * Grace-Blackwell node the copies of a long-context problem take longer than
  * the attention, so the overlap shortens the whole call.
  *
@@ -221,7 +222,7 @@ fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, vo
  *                           host memory.
  *
  * Returns as fa_fwd; all argument checks run before any CUDA call.  The first
- * call on a device creates that device's two copy streams and their events.
+ * call on a device creates that device's four streams and their events.
  * Calls on one device share them, so calls from different host threads are
  * serialised on the copy engines.
  */
@@ -233,8 +234,8 @@ fa_status fa_fwd_from_host(const void *Q_host, const void *K_host, const void *V
                            const int32_t *kv_len, int f16, int groups, void *stream);
 
 /* The group count fa_fwd_from_host uses for groups = 0 on the current
- * device: every group keeps at least three waves of 256-row work items
- * (1 for empty problems). */
+ * device: min(B*H, 8, 256-row work items / SMs), at least 1.  (Groups never
+ * span batches, so a call may run more groups than asked for: at least B.) */
 int fa_fwd_from_host_auto_groups(int B, int H, int N, int D);
 
 /*
