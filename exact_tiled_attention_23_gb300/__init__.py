@@ -23,7 +23,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "
            "fa_device_status", "fa_last_error_detail", "fa_fwd_splitkv",
            "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "FA_MAX_SPLITS",
            "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES", "fa_fwd_f16",
-           "fa_bwd", "fa_bwd_workspace_bytes", "backward",
+           "fa_bwd", "fa_bwd_f16", "fa_bwd_workspace_bytes", "backward", "attention",
            "fa_fwd_from_host", "fa_fwd_from_host_auto_groups", "FA_MAX_HOST_GROUPS", "forward_from_host",
            "forward", "build"]
 
@@ -93,6 +93,8 @@ def load():
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
                                ctypes.c_size_t, vp]
         lib.fa_bwd.restype = i32
+        lib.fa_bwd_f16.argtypes = lib.fa_bwd.argtypes
+        lib.fa_bwd_f16.restype = i32
         lib.fa_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_from_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, f32, vp, i32, i32, vp]
@@ -158,6 +160,13 @@ def fa_fwd_from_host(Q_host, K_host, V_host, O_host, LSE_host, Q_dev, K_dev, V_d
 
 def fa_fwd_from_host_auto_groups(B, H, N, D) -> int:
     return int(load().fa_fwd_from_host_auto_groups(B, H, N, D))
+
+
+def fa_bwd_f16(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, causal, scale, kv_len, workspace,
+               workspace_bytes, stream) -> int:
+    """fp16 backward by recomputation; pointers are device addresses or None."""
+    return int(load().fa_bwd_f16(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, int(bool(causal)),
+                                 float(scale), kv_len, workspace, int(workspace_bytes), stream))
 
 
 def fa_bwd_workspace_bytes(B, H, N, D) -> int:
@@ -309,15 +318,17 @@ def forward_from_host(q, k, v, causal: bool = True, scale=None, kv_len=None, out
 def backward(q, k, v, o, do, lse, causal: bool = True, scale=None, kv_len=None, workspace=None,
              stream=None):
     """(dQ, dK, dV) of sum(O * dO) for O, LSE = forward(q, k, v, ...), bf16
-    CUDA tensors [B, H, N, D] with D a multiple of 8 up to 128 (LSE fp32
-    [B, H, N]).  The workspace (a CUDA
+    or fp16 CUDA tensors [B, H, N, D] with D a multiple of 8 up to 128 (LSE
+    fp32 [B, H, N]).  The workspace (a CUDA
     tensor of at least fa_bwd_workspace_bytes bytes) is allocated here with
     torch when not given."""
     import torch
 
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v, o, do must be bf16 or fp16")
     for x in (q, k, v, o, do):
-        if x.shape != q.shape or x.dtype != torch.bfloat16 or not x.is_cuda:
-            raise ValueError("q, k, v, o, do must be bf16 CUDA tensors of one shape [B, H, N, D]")
+        if x.shape != q.shape or x.dtype != q.dtype or not x.is_cuda:
+            raise ValueError("q, k, v, o, do must be CUDA tensors of one dtype and shape [B, H, N, D]")
     q, k, v, o, do = (x.contiguous() for x in (q, k, v, o, do))
     B, H, N, D = q.shape
     lse = lse.contiguous()
@@ -334,10 +345,46 @@ def backward(q, k, v, o, do, lse, causal: bool = True, scale=None, kv_len=None, 
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
-    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, causal,
-                float("nan") if scale is None else float(scale), kv_ptr, workspace.data_ptr(),
-                workspace.numel() * workspace.element_size(), sp)
+    bwd = fa_bwd_f16 if q.dtype == torch.float16 else fa_bwd
+    st = bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, causal,
+             float("nan") if scale is None else float(scale), kv_ptr, workspace.data_ptr(),
+             workspace.numel() * workspace.element_size(), sp)
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv
+
+
+# ------------------------------------------------------------- autograd
+def _attention_function():
+    import torch
+
+    class _Attention(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale, kv_len):
+            o, lse = forward(q, k, v, causal=causal, scale=scale, kv_len=kv_len)
+            ctx.save_for_backward(q, k, v, o, lse, kv_len)
+            ctx.causal, ctx.scale = causal, scale
+            return o
+
+        @staticmethod
+        def backward(ctx, d_o):
+            q, k, v, o, lse, kv_len = ctx.saved_tensors
+            dq, dk, dv = backward(q, k, v, o, d_o.contiguous(), lse, causal=ctx.causal, scale=ctx.scale,
+                                  kv_len=kv_len)
+            return dq, dk, dv, None, None, None
+
+    return _Attention
+
+
+_ATTENTION = None
+
+
+def attention(q, k, v, causal: bool = True, scale=None, kv_len=None):
+    """softmax(scale * q k^T + mask) v as a differentiable torch operation:
+    the forward is fa_fwd / fa_fwd_f16 and the backward fa_bwd / fa_bwd_f16
+    (bf16 or fp16 CUDA tensors [B, H, N, D], D a multiple of 8 up to 128)."""
+    global _ATTENTION
+    if _ATTENTION is None:
+        _ATTENTION = _attention_function()
+    return _ATTENTION.apply(q, k, v, bool(causal), scale, kv_len)

@@ -192,6 +192,59 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Shared checks and launches of the backward (bf16 or fp16 tensors).
+fa_status bwd16(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                int causal, float scale, const int32_t *kv_len, void *workspace,
+                size_t workspace_bytes, void *stream, bool f16)
+{
+    fa_status st = check_common(Q, K, V, dQ, B, H, N, D);
+    if (st != FA_OK) return st;
+    if ((int64_t)B * H * N == 0) return FA_OK;
+    if (!O || !dO || !LSE || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
+    if (!tc_fwd_head_dim(D)) return FA_ERR_UNSUPPORTED;
+    const void *ptrs16[] = {Q, K, V, O, dO, dQ, dK, dV, workspace};
+    for (const void *ptr : ptrs16)
+        if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(LSE) & 3u) || (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)))
+        return FA_ERR_INVALID_ARG;
+    if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, D)) return FA_ERR_INVALID_ARG;
+    const int64_t ctas = (int64_t)B * H * (((int64_t)N + 127) / 128);
+    if (ctas > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+    const int64_t BH = (int64_t)B * H;
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_map16(&tq, Q, BH, N, D, dt) || !encode_map16(&tk, K, BH, N, D, dt) ||
+        !encode_map16(&tv, V, BH, N, D, dt) || !encode_map16(&tdo, dO, BH, N, D, dt) ||
+        !encode_dq_acc_map(&tdq, workspace, BH, N, D))
+        return FA_ERR_CUDA;
+    fa::BwdParams p{};
+    p.q = Q;
+    p.k = K;
+    p.v = V;
+    p.o = O;
+    p.d_o = dO;
+    p.lse = LSE;
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.kv_len = kv_len;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.D = D;
+    p.causal = causal ? 1 : 0;
+    p.f16 = f16 ? 1 : 0;
+    p.scale = resolve_scale(scale, D);
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.wait_limit_ns = wait_limit_ns();
+    p.dq_acc = static_cast<float *>(workspace);
+    p.delta = p.dq_acc + (size_t)BH * N * D;
+    cudaError_t e = fa::launch_bwd_bf16(p, tq, tk, tv, tdo, tdq, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -291,49 +344,17 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                  int causal, float scale, const int32_t *kv_len, void *workspace,
                  size_t workspace_bytes, void *stream)
 {
-    fa_status st = check_common(Q, K, V, dQ, B, H, N, D);
-    if (st != FA_OK) return st;
-    if ((int64_t)B * H * N == 0) return FA_OK;
-    if (!O || !dO || !LSE || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
-    if (!tc_fwd_head_dim(D)) return FA_ERR_UNSUPPORTED;
-    const void *ptrs16[] = {Q, K, V, O, dO, dQ, dK, dV, workspace};
-    for (const void *ptr : ptrs16)
-        if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(LSE) & 3u) || (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)))
-        return FA_ERR_INVALID_ARG;
-    if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, D)) return FA_ERR_INVALID_ARG;
-    const int64_t ctas = (int64_t)B * H * (((int64_t)N + 127) / 128);
-    if (ctas > INT32_MAX) return FA_ERR_INVALID_ARG;
+    return bwd16(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, causal, scale, kv_len, workspace,
+                 workspace_bytes, stream, false);
+}
 
-    const int64_t BH = (int64_t)B * H;
-    CUtensorMap tq, tk, tv, tdo, tdq;
-    if (!encode_bf16_map(&tq, Q, BH, N, D) || !encode_bf16_map(&tk, K, BH, N, D) ||
-        !encode_bf16_map(&tv, V, BH, N, D) || !encode_bf16_map(&tdo, dO, BH, N, D) ||
-        !encode_dq_acc_map(&tdq, workspace, BH, N, D))
-        return FA_ERR_CUDA;
-    fa::BwdParams p{};
-    p.q = Q;
-    p.k = K;
-    p.v = V;
-    p.o = O;
-    p.d_o = dO;
-    p.lse = LSE;
-    p.dq = dQ;
-    p.dk = dK;
-    p.dv = dV;
-    p.kv_len = kv_len;
-    p.B = B;
-    p.H = H;
-    p.N = N;
-    p.D = D;
-    p.causal = causal ? 1 : 0;
-    p.scale = resolve_scale(scale, D);
-    p.scale_log2 = p.scale * 1.4426950408889634f;
-    p.wait_limit_ns = wait_limit_ns();
-    p.dq_acc = static_cast<float *>(workspace);
-    p.delta = p.dq_acc + (size_t)BH * N * D;
-    cudaError_t e = fa::launch_bwd_bf16(p, tq, tk, tv, tdo, tdq, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+fa_status fa_bwd_f16(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                     int causal, float scale, const int32_t *kv_len, void *workspace,
+                     size_t workspace_bytes, void *stream)
+{
+    return bwd16(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, causal, scale, kv_len, workspace,
+                 workspace_bytes, stream, true);
 }
 
 const char *fa_status_string(fa_status s)

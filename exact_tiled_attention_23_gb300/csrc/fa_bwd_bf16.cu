@@ -12,7 +12,7 @@
 // Kernels, all on the caller's stream:
 //   1. bwd_prep_kernel: Delta per query row (fp32) and a zeroed fp32 dQ
 //      accumulator, both in the caller's workspace;
-//   2. bwd_kernel<D>: one CTA per (batch*head, 128-key tile).  K_j, V_j stay
+//   2. bwd_kernel<D, kF16>: one CTA per (batch*head, 128-key tile).  K_j, V_j stay
 //      in shared memory; the query tiles that see them stream through a
 //      two-stage TMA ring with their dO.  Per query tile, in tensor memory
 //      (one TMEM lane per key):
@@ -29,6 +29,8 @@
 #include "fa_internal.h"
 #include "fa_tc_common.cuh"
 #include "sm103_ptx.cuh"
+
+#include <cuda_fp16.h>
 
 #include <cmath>
 
@@ -65,7 +67,7 @@ struct BwdLayout {
     static_assert(kSmemBytes + 2048 <= 232448, "shared memory budget");
 };
 
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -188,9 +190,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             // chunks one box (16 KiB) apart; a K-step of 16 rows is 2 KiB
             const uint64_t dK_mn = make_sdesc(base + Lay::kKOff, Lay::kChunkBytes, 1024);
             const uint64_t dS_mn = make_sdesc(base + Lay::kDSOff, Lay::kChunkBytes, 1024);
-            constexpr uint32_t id_st = make_idesc(BK, BQ, 0, 0);    // S^T, dP^T: 128 keys x 128 queries
-            constexpr uint32_t id_acc = make_idesc(BK, D, 0, 1);    // dV, dK: A in TMEM, B MN-major
-            constexpr uint32_t id_dq = make_idesc(BQ, D, 1, 1);     // dQ: A = dS MN-major, B = K MN-major
+            constexpr uint32_t id_st = make_idesc(BK, BQ, 0, 0, kF16);   // S^T, dP^T: 128 keys x 128 queries
+            constexpr uint32_t id_acc = make_idesc(BK, D, 0, 1, kF16);   // dV, dK: A in TMEM, B MN-major
+            constexpr uint32_t id_dq = make_idesc(BQ, D, 1, 1, kF16);    // dQ: A = dS MN-major, B = K MN-major
 
             auto issue_dpt = [&](int stage) {   // dP^T = V_j dO_i^T
                 const uint64_t dO_km = make_sdesc(base + Lay::kStageOff + stage * Lay::kStageBytes + Lay::kTileBytes,
@@ -327,8 +329,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                         ptx::unpack2(ptx::mul2(ptx::pack2(p0, p1),
                                                ptx::add2(ptx::pack2(u2f(dpv[2 * e]), u2f(dpv[2 * e + 1])), nd2[e])),
                                      d0, d1);
-                        pw[e] = ptx::pack_bf16x2(p0, p1);
-                        dsw[e] = ptx::pack_bf16x2(d0, d1);
+                        pw[e] = ptx::pack16x2<kF16>(p0, p1);
+                        dsw[e] = ptx::pack16x2<kF16>(d0, d1);
                     }
                 } else {
 #pragma unroll
@@ -338,8 +340,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                         ptx::unpack2(nd2[e], nda, ndb);
                         const float pa = 2 * e >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[2 * e]), sl2, nla)) : 0.f;
                         const float pb = 2 * e + 1 >= e_min ? ptx::ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, nlb)) : 0.f;
-                        pw[e] = ptx::pack_bf16x2(pa, pb);
-                        dsw[e] = ptx::pack_bf16x2(pa * (u2f(dpv[2 * e]) + nda), pb * (u2f(dpv[2 * e + 1]) + ndb));
+                        pw[e] = ptx::pack16x2<kF16>(pa, pb);
+                        dsw[e] = ptx::pack16x2<kF16>(pa * (u2f(dpv[2 * e]) + nda), pb * (u2f(dpv[2 * e + 1]) + ndb));
                     }
                 }
                 ptx::tmem_st16(tmem + lane_off + Lay::kColST + c * 16, pw);
@@ -399,7 +401,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                         uint32_t w[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            w[e] = n_iter > 0 ? ptx::pack_bf16x2(u2f(v[2 * e]) * mul, u2f(v[2 * e + 1]) * mul) : 0u;
+                            w[e] = n_iter > 0 ? ptx::pack16x2<kF16>(u2f(v[2 * e]) * mul, u2f(v[2 * e + 1]) * mul) : 0u;
                         uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -474,6 +476,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 // Delta = rowsum(dO * O) per query row (over the D real columns), and the
 // zeroed fp32 dQ accumulator.  One warp per row.
+template <bool kF16>
+__device__ __forceinline__ float f16_to_f32(uint16_t x)
+{
+    if constexpr (kF16)
+        return __half2float(__ushort_as_half(x));
+    else
+        return __uint_as_float((uint32_t)x << 16);
+}
+
+template <bool kF16>
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ d_o,
                 float *__restrict__ delta, float *__restrict__ dq_acc, int64_t rows, int D)
@@ -484,7 +496,7 @@ bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ d_o
     float s = 0.f;
     for (int c = lane; c < D; c += 32) {
         const int64_t idx = row * D + c;
-        s = fmaf(__uint_as_float((uint32_t)o[idx] << 16), __uint_as_float((uint32_t)d_o[idx] << 16), s);
+        s = fmaf(f16_to_f32<kF16>(o[idx]), f16_to_f32<kF16>(d_o[idx]), s);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -492,17 +504,18 @@ bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ d_o
     for (int c = lane; c < D; c += 32) dq_acc[row * D + c] = 0.f;
 }
 
-// dQ = scale * accumulator, rounded to bf16 (two elements per thread).
+// dQ = scale * accumulator, rounded to bf16 / fp16 (two elements per thread).
+template <bool kF16>
 __global__ void __launch_bounds__(256)
 bwd_dq_kernel(const float *__restrict__ dq_acc, uint16_t *__restrict__ dq, float scale, int64_t n2)
 {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n2) return;
     const float2 v = reinterpret_cast<const float2 *>(dq_acc)[i];
-    reinterpret_cast<uint32_t *>(dq)[i] = ptx::pack_bf16x2(v.x * scale, v.y * scale);
+    reinterpret_cast<uint32_t *>(dq)[i] = ptx::pack16x2<kF16>(v.x * scale, v.y * scale);
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdq,
                          cudaStream_t stream)
@@ -510,23 +523,23 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
     using Lay = BwdLayout<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int64_t rows = p.B * p.H * p.N;
-    bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+    bwd_prep_kernel<kF16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
         static_cast<const uint16_t *>(p.o), static_cast<const uint16_t *>(p.d_o), p.delta, p.dq_acc, rows,
         (int)p.D);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t ctas = p.B * p.H * ((p.N + BK - 1) / BK);
-    bwd_kernel<D><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+    bwd_kernel<D, kF16><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t n2 = rows * p.D / 2;
-    bwd_dq_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t *>(p.dq),
+    bwd_dq_kernel<kF16><<<(unsigned)((n2 + 255) / 256), 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t *>(p.dq),
                                                                   p.scale, n2);
     return cudaGetLastError();
 }
@@ -541,8 +554,11 @@ cudaError_t launch_bwd_bf16(const BwdParams &p, const CUtensorMap &tm_q, const C
     // fill the columns past D with zeros, which adds nothing to any product,
     // and only the D real columns of dQ, dK and dV are written.
     if (p.D % 8 != 0 || p.D <= 0 || p.D > 128) return cudaErrorInvalidValue;
-    if (p.D <= 64) return launch_bwd_d<64>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
-    return launch_bwd_d<128>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
+    if (p.D <= 64)
+        return p.f16 ? launch_bwd_d<64, true>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream)
+                     : launch_bwd_d<64, false>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
+    return p.f16 ? launch_bwd_d<128, true>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream)
+                 : launch_bwd_d<128, false>(p, tm_q, tm_k, tm_v, tm_do, tm_dq, stream);
 }
 
 cudaError_t read_and_clear_status_bwd(uint32_t *out)

@@ -48,7 +48,7 @@ struct FwdParams {
     float *part_lse;
 };
 
-// Arguments of the backward pass (bf16 tensors, fp32 LSE and workspace).
+// Arguments of the backward pass (bf16 or fp16 tensors, fp32 LSE and workspace).
 struct BwdParams {
     const void *q, *k, *v, *o, *d_o;
     const float *lse;
@@ -56,6 +56,7 @@ struct BwdParams {
     const int32_t *kv_len;    // may be null (= N)
     int64_t B, H, N, D;
     int causal;
+    int f16;                  // 16-bit type of Q, K, V, O, dO and the gradients: 0 = bf16, 1 = fp16
     float scale;
     float scale_log2;
     uint64_t wait_limit_ns;

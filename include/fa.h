@@ -261,8 +261,8 @@ int fa_fwd_from_host_auto_groups(int B, int H, int N, int D);
  *                   fa_bwd_workspace_bytes(B,H,N,D) bytes (an fp32 dQ
  *                   accumulator and Delta); fully rewritten by each call;
  *                   calls that may overlap need separate workspaces.
- * dQ is summed across key tiles with fp32 atomic adds, so its last bits may
- * differ from run to run; dK and dV are deterministic.  Four kernels are
+ * dQ is summed across key tiles by fp32 reduce-adds, so its last bits may
+ * differ from run to run; dK and dV are deterministic.  Three kernels are
  * enqueued on `stream`.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a
  * missing or too small workspace.
  */
@@ -270,6 +270,18 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                  const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
                  int causal, float scale, const int32_t *kv_len, void *workspace,
                  size_t workspace_bytes, void *stream);
+
+/*
+ * fa_bwd_f16 -- fa_bwd for the fp16 forward (fa_fwd_f16): IEEE half Q, K, V,
+ * O, dO and dQ, dK, dV; LSE, the workspace and every accumulation stay fp32,
+ * and P and dS are rounded to fp16 for the tensor-core products (P <= 1; dS
+ * must stay inside the fp16 range, as in any fp16 training).  Same arguments,
+ * limits and errors as fa_bwd.
+ */
+fa_status fa_bwd_f16(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D,
+                     int causal, float scale, const int32_t *kv_len, void *workspace,
+                     size_t workspace_bytes, void *stream);
 
 /* Bytes of workspace fa_bwd needs: B*H*N*(D + 1)*4 (0 for invalid sizes). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int D);

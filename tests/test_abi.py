@@ -124,6 +124,8 @@ def test_bwd_workspace_and_argument_checks(lib):
     assert fa.fa_bwd_workspace_bytes(1, 1, -1, 64) == 0
     big = 1 << 40
     assert fa.fa_bwd(P, P, P, P, P, P, P, P, P, 1, 1, 16, 100, 1, NAN, None, P, big, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_f16(P, P, P, P, P, P, P, P, P, 1, 1, 16, 100, 1, NAN, None, P, big, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_f16(P, P, P, None, P, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, P, big, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd(P, P, P, P, P, P, P, P, P, 1, 1, 16, 256, 1, NAN, None, P, big, None) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_bwd(P, P, P, None, P, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, P, big, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd(P, P, P, P, P, P, P, P, P, 1, 1, 16, 64, 1, NAN, None, None, big, None) == fa.FA_ERR_INVALID_ARG

@@ -27,10 +27,10 @@ def built():
     oracle.library()
 
 
-def run_case(B, H, N, D, causal, kv_len, seed):
-    inp = workloads.make_case(B, H, N, D, dtype="bf16", causal=causal, seed=seed, kv_len=kv_len)
+def run_case(B, H, N, D, causal, kv_len, seed, dtype="bf16"):
+    inp = workloads.make_case(B, H, N, D, dtype=dtype, causal=causal, seed=seed, kv_len=kv_len)
     g = torch.Generator("cpu").manual_seed(seed + 77)
-    do = torch.randn((B, H, N, D), generator=g).to(torch.bfloat16)
+    do = torch.randn((B, H, N, D), generator=g).to(inp.q.dtype)
     q, k, v, dog = inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), do.cuda()
     kv = inp.kv_len.cuda() if inp.kv_len is not None else None
     o, lse = fa.forward(q, k, v, causal=causal, kv_len=kv)
@@ -110,3 +110,37 @@ def test_bwd_head_dim_writes_stay_in_bounds(D):
     assert torch.equal(bufs[1][:n].view(B, H, N, D), dk)
     assert torch.equal(bufs[2][:n].view(B, H, N, D), dv)
     assert (bufs[0][:n].view(B, H, N, D).float() - dq.float()).abs().max().item() <= 1e-2 * dq.float().abs().max().item()
+
+
+F16_CASES = [
+    (1, 2, 256, 128, True, None),
+    (2, 1, 300, 64, False, [300, 77]),
+    (1, 1, 257, 96, True, None),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len", F16_CASES)
+def test_bwd_f16_matches_oracle(B, H, N, D, causal, kv_len):
+    """fp16 tensors through fa_bwd_f16 (P and dS rounded to fp16)."""
+    stats = run_case(B, H, N, D, causal, kv_len, seed=N + D + 1, dtype="fp16")
+    print(stats)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_autograd_attention(dtype):
+    """fa.attention is differentiable: torch autograd through it gives the
+    gradients of fa.backward."""
+    inp = workloads.make_case(2, 2, 300, 64, dtype="bf16" if dtype == torch.bfloat16 else "fp16",
+                              causal=True, seed=31, kv_len=[300, 150])
+    kv = inp.kv_len.cuda()
+    q, k, v = (x.cuda().requires_grad_(True) for x in (inp.q, inp.k, inp.v))
+    g = torch.Generator("cpu").manual_seed(5)
+    do = torch.randn(q.shape, generator=g).to(dtype).cuda()
+    o = fa.attention(q, k, v, causal=True, kv_len=kv)
+    (o.float() * do.float()).sum().backward()
+    o2, lse = fa.forward(q.detach(), k.detach(), v.detach(), causal=True, kv_len=kv)
+    dq, dk, dv = fa.backward(q.detach(), k.detach(), v.detach(), o2, do, lse, causal=True, kv_len=kv)
+    torch.cuda.synchronize()
+    assert torch.equal(o.detach(), o2)
+    assert torch.equal(k.grad, dk) and torch.equal(v.grad, dv)
+    assert (q.grad.float() - dq.float()).abs().max().item() <= 1e-2 * dq.float().abs().max().item()
