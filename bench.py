@@ -291,12 +291,13 @@ def run_ours(args, rank, world, local):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)   # outside the timed region
 
     if args.pass_ == "bwd":
-        if w.dtype != "bf16":
-            raise SystemExit("--pass bwd needs a bf16 workload")
+        if w.dtype not in ("bf16", "fp16"):
+            raise SystemExit("--pass bwd needs a bf16 or fp16 workload")
+        bwd = fa.fa_bwd_f16 if w.dtype == "fp16" else fa.fa_bwd
         # the forward's outputs and an upstream gradient, made outside the timed region
         fa.forward(q, k, v, causal=w.causal, kv_len=kv, out=o, lse=lse)
         gen = torch.Generator("cpu").manual_seed(w.seed + 99)
-        d_o = torch.randn(q.shape, generator=gen).to(torch.bfloat16).to(dev)
+        d_o = torch.randn(q.shape, generator=gen).to(q.dtype).to(dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
         bwd_ws_bytes = fa.fa_bwd_workspace_bytes(B, H, N, D)
         bwd_ws = torch.empty(bwd_ws_bytes, dtype=torch.uint8, device=dev)
@@ -304,9 +305,9 @@ def run_ours(args, rank, world, local):
 
     def step():
         if args.pass_ == "bwd":
-            st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(),
-                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
-                           w.causal, float("nan"), kv_ptr, bwd_ws.data_ptr(), bwd_ws_bytes, sp)
+            st = bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(),
+                     lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
+                     w.causal, float("nan"), kv_ptr, bwd_ws.data_ptr(), bwd_ws_bytes, sp)
         elif splits is not None:
             st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                    B, H, N, D, w.causal, float("nan"), kv_ptr, splits,
@@ -462,7 +463,7 @@ def run_ours(args, rank, world, local):
                    "l2": ("256 MiB write before every step (flush not timed)" if flush else
                           "inputs (Q,K,V) larger than L2; no flush between steps"),
                    "parallelism": f"replicas x{world} (no exchange)",
-                   "path": ("fa_bwd" if args.pass_ == "bwd" else
+                   "path": (("fa_bwd_f16" if w.dtype == "fp16" else "fa_bwd") if args.pass_ == "bwd" else
                             "fa_fwd" if splits is None else f"fa_fwd_splitkv (splits={splits})")},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roofline,
