@@ -439,3 +439,36 @@ def test_full_workload(name):
         compare(inp, o, lse)
     else:
         compare(inp, o, lse, rows=sample_rows(inp, seed=w.index))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_key_lengths_out_of_range_are_clamped(D, tiles):
+    """kv_len outside [0, N] is clamped on the device: -5 acts as 0 (every
+    row fully masked: exact zeros, LSE = -inf) and N + 7 as N."""
+    if D == 256 and tiles == "2":
+        pytest.skip("D = 256 always runs the one-tile kernel")
+    inp = workloads.make_case(3, 2, 200, D, dtype="bf16", causal=True, seed=D + 40, kv_len=[-5, 207, 150])
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+    assert bool((o[0] == 0).all()) and bool(torch.isneginf(lse[0]).all())
+
+
+@pytest.mark.parametrize("D", [8, 64, 128, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_single_token(D, dtype):
+    """N = 1: the row attends to itself only, so O = V and LSE = scale q.k
+    ("vectorized-flash-attention-kernel", Evidence & signatures: N=1)."""
+    inp = workloads.make_case(2, 3, 1, D, dtype=dtype, causal=True, seed=D)
+    o, lse = run_gpu(inp)
+    assert torch.equal(o.cpu(), inp.v)
+    ref = inp.scale * (inp.q.float() * inp.k.float()).sum(-1)
+    assert torch.allclose(lse.cpu(), ref, rtol=1e-5, atol=1e-4)
+
+
+def test_d256_ragged_and_padded():
+    """D = 256 with a ragged last tile, key padding with an empty batch and
+    the non-causal mask."""
+    for causal in (True, False):
+        inp = workloads.make_case(3, 2, 333, 256, dtype="bf16", causal=causal, seed=61, kv_len=[333, 0, 129])
+        o, lse = run_gpu(inp)
+        compare(inp, o, lse)
