@@ -181,14 +181,14 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
     if (ctas > INT32_MAX) return FA_ERR_INVALID_ARG;
     const int64_t BH = (int64_t)B * H;
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!encode_map16(&tq, Q, BH, N, D, dt) || !encode_map16(&tk, K, BH, N, D, dt) ||
-        !encode_map16(&tv, V, BH, N, D, dt))
+        !encode_map16(&tv, V, BH, N, D, dt) || !encode_map16(&to, O, BH, N, D, dt))
         return FA_ERR_CUDA;
     fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
     p.f16 = f16 ? 1 : 0;
     cudaError_t e = one_tile ? fa::launch_fwd_onetile(p, tq, tk, tv, static_cast<cudaStream_t>(stream))
-                             : fa::launch_fwd_bf16(p, tq, tk, tv, static_cast<cudaStream_t>(stream));
+                             : fa::launch_fwd_bf16(p, tq, tk, tv, to, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

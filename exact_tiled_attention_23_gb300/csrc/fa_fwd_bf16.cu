@@ -76,7 +76,8 @@ struct Layout {
 template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int q_pairs)
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                const FwdParams p, const int q_pairs)
 {
     using Lay = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -310,10 +311,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
         // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----------------
         bool have = (n_kv > 0) && ok;
-        if (have) {
-            const bool got = wait_bounded(&o_final[i], 0, p.wait_limit_ns, kSiteOFinal, ab);
-            have = __all_sync(0xffffffffu, got);
-        }
+        if (have) have = wait_bounded(&o_final[i], 0, p.wait_limit_ns, kSiteOFinal, ab);
+        // the tile's four warps agree, so that its named barrier below is
+        // reached by all of them or by none
+        have = ptx::bar_and(1 + i, 128, have);
         if (have || n_kv == 0) {
             ptx::tc_fence_after();
             const bool empty = !(l > 0.f);
@@ -323,41 +324,71 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // memory; the rest of the D computed ones are the zero padding.
             const int Dv = (int)p.D;
             const int64_t flat = bh * N + row;
-            uint16_t *orow = static_cast<uint16_t *>(p.o) + flat * Dv;
-            float *prow = kSplit ? p.part_o + ((int64_t)split * BH * N + flat) * Dv : nullptr;
+            if constexpr (kSplit) {
+                float *prow = p.part_o + ((int64_t)split * BH * N + flat) * Dv;
 #pragma unroll 1
-            for (int c = 0; c < D / 32 && c * 32 < Dv; ++c) {
-                uint32_t o[32];
-                if (n_kv > 0) {
-                    ptx::tmem_ld32(tO + c * 32, o);
-                    ptx::tmem_wait_ld();
-                }
-                if (row < N) {
-                    uint32_t w[16];
-                    float f[32];
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        float lo, hi;
-                        ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])),
-                                               ptx::pack2(inv, inv)), lo, hi);
-                        f[2 * t] = empty ? 0.f : lo;
-                        f[2 * t + 1] = empty ? 0.f : hi;
-                        w[t] = empty ? 0u : ptx::pack16x2<kF16>(lo, hi);
+                for (int c = 0; c < D / 32 && c * 32 < Dv; ++c) {
+                    uint32_t o[32];
+                    if (n_kv > 0) {
+                        ptx::tmem_ld32(tO + c * 32, o);
+                        ptx::tmem_wait_ld();
                     }
-                    if (kSplit) {
+                    if (row < N) {
+                        float f[32];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            float lo, hi;
+                            ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])),
+                                                   ptx::pack2(inv, inv)), lo, hi);
+                            f[2 * t] = empty ? 0.f : lo;
+                            f[2 * t + 1] = empty ? 0.f : hi;
+                        }
                         // normalised fp32 partial output of this key range
                         float4 *dst = reinterpret_cast<float4 *>(prow + c * 32);
 #pragma unroll
                         for (int t = 0; t < 8; ++t)
                             if (c * 32 + 4 * t < Dv)
                                 dst[t] = make_float4(f[4 * t], f[4 * t + 1], f[4 * t + 2], f[4 * t + 3]);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            if (c * 32 + 8 * t < Dv)
-                                dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                     }
+                }
+            } else {
+                // O = acc / l as 16-bit, staged in this tile's Q buffer (free:
+                // every MMA has completed) as 128-byte-swizzled 128 x 64 boxes,
+                // then written by TMA stores that clip rows >= N and columns
+                // >= p.D.
+                uint8_t *obuf = smem + Lay::kQOff + i * Lay::kTileBytes;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    if (n_kv > 0) {
+                        ptx::tmem_ld32(tO + c * 32, o);
+                        ptx::tmem_wait_ld();
+                    }
+                    uint32_t w[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        float lo = 0.f, hi = 0.f;
+                        if (n_kv > 0)
+                            ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])), ptx::pack2(inv, inv)),
+                                         lo, hi);
+                        w[t] = empty ? 0u : ptx::pack16x2<kF16>(lo, hi);
+                    }
+                    // 32 columns = 4 of the 8 16-byte units of a 64-column box row
+                    const uint32_t row_addr = ptx::smem_u32(obuf + (c / 2) * Lay::kChunkBytes + r_local * 128);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t unit = (uint32_t)((c % 2) * 4 + u) ^ (uint32_t)(r_local & 7);
+                        ptx::st_shared_v4(row_addr + (unit << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::bar_sync(1 + i, 128);                 // this tile's four warps
+                if (r_local == 0) {
+                    for (int c = 0; c < Lay::kChunks; ++c)
+                        ptx::tma_store_3d(&tm_o, obuf + c * Lay::kChunkBytes, c * 64, (int32_t)(q0 + i * BM),
+                                          (int32_t)bh);
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_group_read<0>();       // the boxes have left shared memory
                 }
             }
             if (row < N) {
@@ -379,7 +410,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D, bool kSplit, bool kF16>
 cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, cudaStream_t stream)
+                     const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t stream)
 {
     using Lay = Layout<D>;
     static bool configured = false;
@@ -392,7 +423,8 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
     }
     const int q_pairs = (int)((p.N + 2 * BM - 1) / (2 * BM));
     const int64_t ctas = p.B * p.H * (int64_t)q_pairs * (kSplit ? p.num_splits : 1);
-    fwd_bf16_kernel<D, kSplit, kF16><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_pairs);
+    fwd_bf16_kernel<D, kSplit, kF16><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, to, p,
+                                                                                           q_pairs);
     return cudaGetLastError();
 }
 
@@ -462,7 +494,7 @@ template <int D, bool kF16>
 cudaError_t launch_split(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, cudaStream_t stream)
 {
-    cudaError_t e = launch_d<D, true, kF16>(p, tq, tk, tv, stream);
+    cudaError_t e = launch_d<D, true, kF16>(p, tq, tk, tv, tq, stream);   // tq: no O map is read
     if (e != cudaSuccess) return e;
     const int64_t rows = p.B * p.H * p.N;
     merge_splits_kernel<D, kF16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
@@ -477,14 +509,14 @@ cudaError_t launch_split(const FwdParams &p, const CUtensorMap &tq, const CUtens
 // which leaves every score unchanged, and the padded output columns are never
 // stored.
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                            const CUtensorMap &tm_v, cudaStream_t stream)
+                            const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t stream)
 {
     if (p.D % 8 != 0 || p.D <= 0 || p.D > 128) return cudaErrorInvalidValue;
     if (p.D <= 64)
-        return p.f16 ? launch_d<64, false, true>(p, tm_q, tm_k, tm_v, stream)
-                     : launch_d<64, false, false>(p, tm_q, tm_k, tm_v, stream);
-    return p.f16 ? launch_d<128, false, true>(p, tm_q, tm_k, tm_v, stream)
-                 : launch_d<128, false, false>(p, tm_q, tm_k, tm_v, stream);
+        return p.f16 ? launch_d<64, false, true>(p, tm_q, tm_k, tm_v, tm_o, stream)
+                     : launch_d<64, false, false>(p, tm_q, tm_k, tm_v, tm_o, stream);
+    return p.f16 ? launch_d<128, false, true>(p, tm_q, tm_k, tm_v, tm_o, stream)
+                 : launch_d<128, false, false>(p, tm_q, tm_k, tm_v, tm_o, stream);
 }
 
 cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,

@@ -67,7 +67,7 @@ struct BwdParams {
 // Launchers (return the CUDA error of the launch).
 cudaError_t launch_fwd_fp32(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                            const CUtensorMap &tm_v, cudaStream_t stream);
+                            const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t stream);
 
 // One 128-row query tile per CTA: head dimension 256, and grids too small for
 // the two-tile kernel to fill the GPU.

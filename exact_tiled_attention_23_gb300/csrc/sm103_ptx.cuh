@@ -370,6 +370,17 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, const void *
         : "memory");
 }
 
+// Tiled TMA store of a shared-memory box to global memory (rows and columns
+// outside the tensor are not written).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, int32_t x, int32_t y,
+                                             int32_t z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
