@@ -187,7 +187,7 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
         return FA_ERR_CUDA;
     fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
     p.f16 = f16 ? 1 : 0;
-    cudaError_t e = one_tile ? fa::launch_fwd_onetile(p, tq, tk, tv, static_cast<cudaStream_t>(stream))
+    cudaError_t e = one_tile ? fa::launch_fwd_onetile(p, tq, tk, tv, to, static_cast<cudaStream_t>(stream))
                              : fa::launch_fwd_bf16(p, tq, tk, tv, to, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

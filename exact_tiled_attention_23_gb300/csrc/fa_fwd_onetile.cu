@@ -65,7 +65,8 @@ __device__ __forceinline__ uint32_t col_s(int buf) { return (uint32_t)buf * 128u
 template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int q_tiles)
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const FwdParams p, const int q_tiles)
 {
     using Lay = OneTileLayout<D>;
     constexpr int kChunks = Lay::kChunks, kTileBytes = Lay::kTileBytes;
@@ -261,10 +262,10 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
         // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----------------
         bool have = (n_kv > 0) && ok;
-        if (have) {
-            const bool got = wait_bounded(o_final, 0, p.wait_limit_ns, kSiteOFinal, ab);
-            have = __all_sync(0xffffffffu, got);
-        }
+        if (have) have = wait_bounded(o_final, 0, p.wait_limit_ns, kSiteOFinal, ab);
+        // the four softmax warps agree, so that the named barrier below is
+        // reached by all of them or by none
+        have = ptx::bar_and(1, 128, have);
         if (have || n_kv == 0) {
             ptx::tc_fence_after();
             const bool empty = !(st.l > 0.f);
@@ -274,29 +275,42 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // memory; the rest of the D computed ones are the zero padding.
             const int Dv = (int)p.D;
             const int64_t flat = bh * N + row;
-            uint16_t *orow = static_cast<uint16_t *>(p.o) + flat * Dv;
+            (void)Dv;
+            // O = acc / l as 16-bit, staged in the Q buffer (free: every MMA
+            // has completed) as 128-byte-swizzled 128 x 64 boxes, then written
+            // by TMA stores that clip rows >= N and columns >= p.D.
+            uint8_t *obuf = smem + kQOff;
 #pragma unroll 1
-            for (int c = 0; c < D / 32 && c * 32 < Dv; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 if (n_kv > 0) {
                     ptx::tmem_ld32(tO + c * 32, o);
                     ptx::tmem_wait_ld();
                 }
-                if (row < N) {
-                    uint32_t w[16];
+                uint32_t w[16];
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        float lo, hi;
+                for (int t = 0; t < 16; ++t) {
+                    float lo = 0.f, hi = 0.f;
+                    if (n_kv > 0)
                         ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])), ptx::pack2(inv, inv)),
                                      lo, hi);
-                        w[t] = empty ? 0u : ptx::pack16x2<kF16>(lo, hi);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (c * 32 + 8 * t < Dv)
-                            dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                    w[t] = empty ? 0u : ptx::pack16x2<kF16>(lo, hi);
                 }
+                // 32 columns = 4 of the 8 16-byte units of a 64-column box row
+                const uint32_t row_addr = ptx::smem_u32(obuf + (c / 2) * kChunkBytes + r_local * 128);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t unit = (uint32_t)((c % 2) * 4 + u) ^ (uint32_t)(r_local & 7);
+                    ptx::st_shared_v4(row_addr + (unit << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::bar_sync(1, 128);                         // the four softmax warps
+            if (r_local == 0) {
+                for (int c = 0; c < kChunks; ++c)
+                    ptx::tma_store_3d(&tm_o, obuf + c * kChunkBytes, c * 64, (int32_t)q0, (int32_t)bh);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read<0>();           // the boxes have left shared memory
             }
             if (row < N && p.lse) p.lse[flat] = lse_row;
         }
@@ -312,7 +326,7 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 template <int D, bool kF16>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                   cudaStream_t stream)
+                   const CUtensorMap &to, cudaStream_t stream)
 {
     using Lay = OneTileLayout<D>;
     static bool configured = false;
@@ -324,15 +338,15 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
     }
     const int q_tiles = (int)((p.N + BM - 1) / BM);
     const int64_t ctas = p.B * p.H * (int64_t)q_tiles;
-    fwd_onetile_kernel<D, kF16><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, p, q_tiles);
+    fwd_onetile_kernel<D, kF16><<<(unsigned)ctas, kThreads, Lay::kSmemBytes, stream>>>(tq, tk, tv, to, p, q_tiles);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_f(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                     cudaStream_t stream)
+                     const CUtensorMap &to, cudaStream_t stream)
 {
-    return p.f16 ? launch<D, true>(p, tq, tk, tv, stream) : launch<D, false>(p, tq, tk, tv, stream);
+    return p.f16 ? launch<D, true>(p, tq, tk, tv, to, stream) : launch<D, false>(p, tq, tk, tv, to, stream);
 }
 
 }  // namespace
@@ -340,12 +354,12 @@ cudaError_t launch_f(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
 // D = 256, or a multiple of 8 up to 128 run at the next of 64 / 128 with
 // zero-filled columns (as in the two-tile kernel).
 cudaError_t launch_fwd_onetile(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                               const CUtensorMap &tm_v, cudaStream_t stream)
+                               const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t stream)
 {
-    if (p.D == 256) return launch_f<256>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D == 256) return launch_f<256>(p, tm_q, tm_k, tm_v, tm_o, stream);
     if (p.D % 8 != 0 || p.D <= 0 || p.D > 128) return cudaErrorInvalidValue;
-    if (p.D <= 64) return launch_f<64>(p, tm_q, tm_k, tm_v, stream);
-    return launch_f<128>(p, tm_q, tm_k, tm_v, stream);
+    if (p.D <= 64) return launch_f<64>(p, tm_q, tm_k, tm_v, tm_o, stream);
+    return launch_f<128>(p, tm_q, tm_k, tm_v, tm_o, stream);
 }
 
 cudaError_t read_and_clear_status_onetile(uint32_t *out)

@@ -72,7 +72,7 @@ cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const C
 // One 128-row query tile per CTA: head dimension 256, and grids too small for
 // the two-tile kernel to fill the GPU.
 cudaError_t launch_fwd_onetile(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                            const CUtensorMap &tm_v, cudaStream_t stream);
+                               const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t stream);
 
 // Split-KV forward: partial kernel over key-block ranges, then the merge.
 cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
