@@ -1,13 +1,19 @@
-"""Exact tiled attention forward for GB300 -- Python binding of libfa.so.
+"""Exact tiled attention for GB300 -- Python binding of libfa.so.
 
-The functions named like the C ABI (``fa_fwd``, ``fa_fwd_fp32``,
-``fa_status_string``, ``fa_device_status``, ``fa_last_error_detail``) take
-raw device pointers and sizes exactly as declared in ``include/fa.h`` and only
-marshal arguments through ctypes.  ``forward()`` is the convenience call on
-torch tensors: it checks shapes, allocates O and LSE with torch, and calls the
-same entry points on the current CUDA stream.  Every step of the computation
-runs in the library's CUDA kernels; there is no other code path, and calling
-without the built library raises.
+The functions named like the C ABI (``fa_fwd``, ``fa_fwd_f16``,
+``fa_fwd_fp32``, ``fa_fwd_splitkv``, ``fa_fwd_splitkv_noalloc``,
+``fa_fwd_from_host``, ``fa_bwd``, ``fa_bwd_f16``, the workspace and status
+helpers) take raw pointers and sizes exactly as declared in ``include/fa.h``
+and only marshal arguments through ctypes.  The torch conveniences on top:
+
+* ``forward()`` -- O, LSE for CUDA tensors (allocates O and LSE with torch);
+* ``forward_from_host()`` -- the same for CPU tensors, copies overlapped with
+  the computation;
+* ``backward()`` -- dQ, dK, dV by recomputation;
+* ``attention()`` -- a differentiable torch operation (forward + backward).
+
+Every step of the computation runs in the library's CUDA kernels; there is no
+other code path, and calling without the built library raises.
 """
 from __future__ import annotations
 
@@ -203,9 +209,10 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
     """O, LSE = attention(q, k, v) for CUDA tensors of shape [B, H, N, D].
 
     bf16 and fp16 inputs use the tensor-core path (D a multiple of 8 up to
-    128, or 256); fp32 inputs use the fp32 path (D <= 256).  scale=None selects 1/sqrt(D).  kv_len: optional
-    int32 CUDA tensor [B] of key lengths.  Runs asynchronously on `stream`
-    (default: torch's current stream).
+    128, or 256); fp32 inputs use the fp32 path (D <= 256).  scale=None
+    selects 1/sqrt(D).  kv_len: optional int32 CUDA tensor [B] of key
+    lengths.  Runs asynchronously on `stream` (default: torch's current
+    stream).
 
     splits: None for fa_fwd; an integer (0 = automatic) selects the split-KV
     path (bf16 only), whose workspace is `workspace` (a CUDA tensor of at

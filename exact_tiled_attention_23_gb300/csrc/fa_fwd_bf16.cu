@@ -9,7 +9,8 @@
 //     128-row query tiles; each tile's scores S = Q K_j^T and output O live in
 //     tensor memory (one TMEM lane per query row, fp32);
 //   * warp 0 streams Q once and K_j, V_j through a ring of shared-memory slots
-//     with TMA (128-byte swizzled boxes of 128 rows x 64 columns);
+//     with TMA (128-byte swizzled boxes of 128 rows x 64 columns; a head
+//     dimension below 64 / 128 reads zero-filled columns);
 //   * warp 1 issues every tcgen05.mma: S_i = Q_i K_j^T (both operands in
 //     shared memory) and O_i += P_i V_j (P_i read from tensor memory);
 //   * warps 4-7 and 8-11 run the online softmax of tile 0 and tile 1: each
@@ -17,7 +18,13 @@
 //     and sum l, writes P_i = exp2(S*scale*log2e - m) as bf16 back into the
 //     same TMEM columns, and rescales O_i in TMEM when the max moved;
 //   * while one tile's softmax runs, the tensor core works on the other tile,
-//     so the two softmax warpgroups alternate with the MMAs.
+//     so the two softmax warpgroups alternate with the MMAs;
+//   * at the end each tile's warps stage O (16-bit) in the tile's Q buffer and
+//     one thread writes it with TMA stores (split-KV partials, fp32, are
+//     stored by the threads).
+//
+// The one-tile kernel (fa_fwd_onetile.cu) serves D = 256 and small grids;
+// both share the per-row softmax step of fa_fwd_softmax.cuh.
 //
 // The reference max is lazy: after the first key block it moves only when a
 // block's sum of p exceeds 2^64, so almost every block needs no max scan and
