@@ -34,6 +34,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -82,13 +83,19 @@ KERNEL_SOURCES = {
 }
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the kernel's sources with comments and blank space removed, so
+    that editing a comment keeps profiled counters valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_23_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            code = _COMMENT.sub("", f.read())
+        h.update(name.encode())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 
