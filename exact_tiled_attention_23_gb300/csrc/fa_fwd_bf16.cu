@@ -206,24 +206,30 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t q_base = ptx::smem_u32(smem + Lay::kQOff);
             const uint32_t kv_base = ptx::smem_u32(smem + Lay::kKVOff);
 
+            // The start-address field of a descriptor is the byte address / 16,
+            // and every operand lies below 256 KiB, so moving an operand by a
+            // byte offset moves its descriptor by offset / 16: the descriptors
+            // are built once here, and each K-step adds a constant.
+            const uint64_t q_desc = make_sdesc(q_base, 16, 1024);            // K-major Q tiles
+            const uint64_t k_desc = make_sdesc(kv_base, 16, 1024);           // K-major K slots
+            const uint64_t v_desc = make_sdesc(kv_base, Lay::kChunkBytes, 1024);   // MN-major V slots
+            constexpr uint64_t kTileStep = Lay::kTileBytes >> 4;
             auto issue_s = [&](int i, int slot) {
-                const uint32_t qa = q_base + i * Lay::kTileBytes;
-                const uint32_t ka = kv_base + slot * Lay::kTileBytes;
+                const uint64_t qd = q_desc + (uint64_t)i * kTileStep;
+                const uint64_t kd = k_desc + (uint64_t)slot * kTileStep;
+                const uint32_t ts = tmem + Lay::col_s(i);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * Lay::kChunkBytes + (k % 4) * 32;
-                    ptx::mma_ss(tmem + Lay::col_s(i), make_sdesc(qa + off, 16, 1024),
-                                make_sdesc(ka + off, 16, 1024), idesc_qk, k > 0);
+                    const uint64_t off = (uint64_t)(((k / 4) * Lay::kChunkBytes + (k % 4) * 32) >> 4);
+                    ptx::mma_ss(ts, qd + off, kd + off, idesc_qk, k > 0);
                 }
             };
             auto issue_pv = [&](int i, int slot, uint32_t acc) {
-                const uint32_t va = kv_base + slot * Lay::kTileBytes;
+                const uint64_t vd = v_desc + (uint64_t)slot * kTileStep;
+                const uint32_t to = tmem + Lay::col_o(i), ts = tmem + Lay::col_s(i);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    ptx::mma_ts(tmem + Lay::col_o(i), tmem + Lay::col_s(i) + k * 8,
-                                make_sdesc(va + k * 2048, Lay::kChunkBytes, 1024), idesc_pv,
-                                (acc | (uint32_t)k) != 0);
-                }
+                for (int k = 0; k < BN / 16; ++k)
+                    ptx::mma_ts(to, ts + k * 8, vd + (uint64_t)((k * 2048) >> 4), idesc_pv, (acc | (uint32_t)k) != 0);
             };
 
             bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&

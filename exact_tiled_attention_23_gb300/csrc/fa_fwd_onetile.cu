@@ -169,18 +169,23 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint32_t qa = ptx::smem_u32(smem + kQOff);
             const uint32_t ka = ptx::smem_u32(smem + kKOff);
             const uint32_t va = ptx::smem_u32(smem + kVOff);
+            // The start-address field of a descriptor is the byte address / 16,
+            // and every operand lies below 256 KiB: the descriptors are built
+            // once, and each K-step adds its byte offset / 16.
+            const uint64_t q_desc = make_sdesc(qa, 16, 1024);
+            const uint64_t k_desc = make_sdesc(ka, 16, 1024);
+            const uint64_t v_desc = make_sdesc(va, kChunkBytes, 1024);
             auto issue_s = [&](int buf) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * kChunkBytes + (k % 4) * 32;
-                    ptx::mma_ss(tmem + col_s(buf), make_sdesc(qa + off, 16, 1024), make_sdesc(ka + off, 16, 1024),
-                                idesc_qk, k > 0);
+                    const uint64_t off = (uint64_t)(((k / 4) * kChunkBytes + (k % 4) * 32) >> 4);
+                    ptx::mma_ss(tmem + col_s(buf), q_desc + off, k_desc + off, idesc_qk, k > 0);
                 }
             };
             auto issue_pv = [&](int buf, bool acc) {
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                    ptx::mma_ts(tmem + kColO, tmem + col_s(buf) + k * 8, make_sdesc(va + k * 2048, kChunkBytes, 1024),
+                    ptx::mma_ts(tmem + kColO, tmem + col_s(buf) + k * 8, v_desc + (uint64_t)((k * 2048) >> 4),
                                 idesc_pv, acc || k > 0);
             };
             bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
