@@ -468,7 +468,8 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "causal": w.causal,
                    "padded": w.padded, "flops_per_step": flops, "unmasked_pairs": pairs,
                    "l2": ("256 MiB write before every step (flush not timed)" if flush else
-                          "inputs (Q,K,V) larger than L2; no flush between steps"),
+                          "inputs (Q,K,V) larger than L2; no flush between steps" if input_bytes >= L2_BYTES else
+                          f"no flush: inputs (Q,K,V, {input_bytes >> 20} MiB) stay in L2 between steps (warm)"),
                    "parallelism": f"replicas x{world} (no exchange)",
                    "path": (("fa_bwd_f16" if w.dtype == "fp16" else "fa_bwd") if args.pass_ == "bwd" else
                             "fa_fwd" if splits is None else f"fa_fwd_splitkv (splits={splits})")},
