@@ -64,6 +64,12 @@ struct Layout {
     static constexpr int kChunkBytes = BM * 128;      // one 128 x 64 bf16 box
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kSlots = (D == 64) ? 8 : 4;  // K/V ring depth (K_j, V_j alternate)
+    // Arrival barriers, one per (V_{j-1}, K_j) pair, used round-robin.  Pair m
+    // is armed by its V tile, whose slot frees only after the MMA warp has
+    // waited on pair m - kSlots/2; one barrier more than that distance makes
+    // pair m's barrier the one of pair m - kSlots/2 - 1, already consumed.
+    // (Pairs up to kSlots/2 fill fresh slots and take fresh barriers.)
+    static constexpr int kPairBars = kSlots / 2 + 1;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
@@ -76,7 +82,7 @@ struct Layout {
     __device__ static constexpr uint32_t col_o(int i) { return 256u + (uint32_t)i * D; }
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert((1 + 2 * kSlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((1 + kPairBars + kSlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 
@@ -92,8 +98,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
     uint64_t *q_full = bars;
-    uint64_t *slot_full = bars + 1;
-    uint64_t *slot_empty = slot_full + Lay::kSlots;
+    // K/V arrivals are grouped as the MMA warp consumes them: PV(j) reads V_j
+    // and the S(j+1) issued right after it reads K_{j+1}, so one barrier
+    // covers the pair (V_j, K_{j+1}) -- "pair j+1" -- and K_0 alone is pair 0.
+    uint64_t *pair_full = bars + 1;                      // [kPairBars]
+    uint64_t *slot_empty = pair_full + Lay::kPairBars;   // [kSlots]
     uint64_t *s_full = slot_empty + Lay::kSlots;   // [2]
     uint64_t *p_full = s_full + 2;                 // [2]
     uint64_t *o_final = p_full + 2;                // [2]
@@ -130,10 +139,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- set-up -----------------------------------------------------------
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
-        for (int s = 0; s < Lay::kSlots; ++s) {
-            ptx::mbar_init(&slot_full[s], 1);
-            ptx::mbar_init(&slot_empty[s], 1);
-        }
+        for (int s = 0; s < Lay::kPairBars; ++s) ptx::mbar_init(&pair_full[s], 1);
+        for (int s = 0; s < Lay::kSlots; ++s) ptx::mbar_init(&slot_empty[s], 1);
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s_full[i], 1);
             ptx::mbar_init(&p_full[i], 4 * 32);
@@ -169,7 +176,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int c = 0; c < Lay::kChunks; ++c)
                     ptx::tma_load_3d(smem + Lay::kQOff + i * Lay::kTileBytes + c * Lay::kChunkBytes,
                                      &tm_q, q_full, c * 64, (int32_t)(q0 + i * BM), (int32_t)bh);
-            uint32_t issued_mask = 0, last_parity = 0;   // per slot, for the final drain
+            int pairs_armed = 0;    // pairs 0 .. pairs_armed-1 have had tiles issued
+            int open_pair = -1;     // a pair whose first tile went out without its arrival
             bool ok = true;
             for (int j = 0; j < n_kv && ok; ++j) {
                 for (int w = 0; w < 2; ++w) {
@@ -182,21 +190,31 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&slot_full[slot], Lay::kTileBytes);
+                    // K_j is pair j (after V_{j-1}); V_j opens pair j+1, which
+                    // K_{j+1} closes -- or V_j alone when it is the last block
+                    const int m = j + w;
+                    uint64_t *bar = &pair_full[m % Lay::kPairBars];
+                    const bool closes = (w == 0) || (j + 1 == n_kv);
+                    if (closes)
+                        ptx::mbar_arrive_expect_tx(bar, Lay::kTileBytes);
+                    else
+                        ptx::mbar_expect_tx(bar, Lay::kTileBytes);
                     const CUtensorMap *tm = w ? &tm_v : &tm_k;
                     for (int c = 0; c < Lay::kChunks; ++c)
                         ptx::tma_load_3d(smem + Lay::kKVOff + slot * Lay::kTileBytes + c * Lay::kChunkBytes,
-                                         tm, &slot_full[slot], c * 64, (int32_t)((blk0 + j) * BN), (int32_t)bh);
-                    issued_mask |= 1u << slot;
-                    last_parity = (last_parity & ~(1u << slot)) | ((uint32_t)(round & 1) << slot);
+                                         tm, bar, c * 64, (int32_t)((blk0 + j) * BN), (int32_t)bh);
+                    open_pair = closes ? -1 : m;
+                    pairs_armed = m + 1;
                 }
             }
+            // A give-up between the two tiles of a pair: close it, so that its
+            // phase completes once the tile in flight has landed.
+            if (open_pair >= 0) ptx::mbar_arrive(&pair_full[open_pair % Lay::kPairBars]);
             // Drain: no copy may still be landing in shared memory at exit.
             wait_bounded(q_full, 0, p.wait_limit_ns, kSiteDrain, ab, false);
-            for (int s = 0; s < Lay::kSlots; ++s)
-                if (issued_mask & (1u << s))
-                    wait_bounded(&slot_full[s], (last_parity >> s) & 1, p.wait_limit_ns, kSiteDrain,
-                                 ab, false);
+            for (int m = pairs_armed > Lay::kPairBars ? pairs_armed - Lay::kPairBars : 0; m < pairs_armed; ++m)
+                wait_bounded(&pair_full[m % Lay::kPairBars], (m / Lay::kPairBars) & 1, p.wait_limit_ns,
+                             kSiteDrain, ab, false);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
@@ -233,7 +251,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             };
 
             bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
-                      wait_bounded(&slot_full[0], 0, p.wait_limit_ns, kSiteSlotFull, ab);
+                      wait_bounded(&pair_full[0], 0, p.wait_limit_ns, kSiteSlotFull, ab);
             if (ok) {
                 ptx::tc_fence_after();
                 issue_s(0, 0);
@@ -243,21 +261,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ptx::mma_commit(&slot_empty[0]);
             }
             for (int j = 0; j < n_kv && ok; ++j) {
-                const int idx_v = 2 * j + 1, slot_v = idx_v % Lay::kSlots;
-                const int idx_k = 2 * j + 2, slot_k = idx_k % Lay::kSlots;
+                const int slot_v = (2 * j + 1) % Lay::kSlots, slot_k = (2 * j + 2) % Lay::kSlots;
                 const bool more = (j + 1 < n_kv);
-                if (!wait_bounded(&slot_full[slot_v], (idx_v / Lay::kSlots) & 1, p.wait_limit_ns,
-                                  kSiteSlotFull, ab) ||
+                // pair j+1: V_j, and K_{j+1} when there is a next block
+                if (!wait_bounded(&pair_full[(j + 1) % Lay::kPairBars], ((j + 1) / Lay::kPairBars) & 1,
+                                  p.wait_limit_ns, kSiteSlotFull, ab) ||
                     !wait_bounded(&p_full[0], j & 1, p.wait_limit_ns, kSitePFull, ab))
                     break;
                 ptx::tc_fence_after();
                 issue_pv(0, slot_v, j > 0);
                 if (!more) ptx::mma_commit(&o_final[0]);
                 if (more) {
-                    if (!wait_bounded(&slot_full[slot_k], (idx_k / Lay::kSlots) & 1, p.wait_limit_ns,
-                                      kSiteSlotFull, ab))
-                        break;
-                    ptx::tc_fence_after();
                     issue_s(0, slot_k);
                     ptx::mma_commit(&s_full[0]);
                 }
