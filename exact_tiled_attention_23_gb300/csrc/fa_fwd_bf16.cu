@@ -143,7 +143,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < Lay::kSlots; ++s) ptx::mbar_init(&slot_empty[s], 1);
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s_full[i], 1);
-            ptx::mbar_init(&p_full[i], 4 * 32);
+            ptx::mbar_init(&p_full[i], 4);          // one arrival per softmax warp
             ptx::mbar_init(&o_final[i], 1);
         }
         ptx::mbar_init(mma_drain, 1);
@@ -331,8 +331,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // O_i is never being written here: s_full[i] for block j is
             // committed after PV_i of block j-1.
             st.block(s_raw, sl2, j > 0, tS, tO, [] {});
+            // every lane's P stores have landed (block() waited for them);
+            // after the warp has synchronised, one lane tells the MMA warp
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&p_full[i]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p_full[i]);
         }
         const float l = st.l, m_ref = st.m_ref;
 

@@ -108,8 +108,8 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int n_kv = (int)((kv_end + BN - 1) / BN);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 12; ++i)   // p_full: one arrival per softmax thread; the rest: one
-            ptx::mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? 4 * 32 : 1);
+        for (int i = 0; i < 12; ++i)   // p_full: one arrival per softmax warp; the rest: one
+            ptx::mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? 4 : 1);
         *abort_word = 0;
         ptx::fence_mbarrier_init();
     }
@@ -257,8 +257,11 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 hook_ok = wait_bounded(pv_done, (j - 1) & 1, p.wait_limit_ns, kSiteOFinal, ab);
                 ptx::tc_fence_after();
             });
+            // every lane's P stores have landed; after the warp has
+            // synchronised, one lane tells the MMA warp
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&p_full[buf]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p_full[buf]);
             if (!__all_sync(0xffffffffu, hook_ok)) {
                 ok = false;
                 break;
