@@ -43,18 +43,27 @@ struct Abort {
     uint32_t *status;
 };
 
+// Drains (waits that do not follow the abort flag) wait for copies and MMAs
+// the CTA itself has in flight, which always end: they keep at least this
+// budget whatever the caller's limit, so a CTA never exits, or frees TMEM,
+// while its own copies or MMAs are still running.
+constexpr uint64_t kDrainFloorNs = 1000000000ull;
+
 // Bounded wait on phase `parity` of `bar`.  Returns false when the budget ran
 // out (the status word records `site`) or, if `follow_abort`, as soon as
-// another thread of the CTA has aborted.
+// another thread of the CTA has aborted.  Budgets below 100 us are checked on
+// every probe, so that a short limit runs out as soon as it is exceeded.
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                              uint32_t site, Abort ab, bool follow_abort = true)
 {
     if (ptx::mbar_test(bar, parity)) return true;
+    if (!follow_abort && limit_ns < kDrainFloorNs) limit_ns = kDrainFloorNs;
+    const uint32_t check_mask = limit_ns < 100000ull ? 0u : 63u;
     const uint64_t t0 = ptx::globaltimer_ns();
     uint32_t spins = 0;
     while (true) {
         if (ptx::mbar_test(bar, parity)) return true;
-        if ((++spins & 63u) == 0) {
+        if ((++spins & check_mask) == 0) {
             if (follow_abort && *ab.flag) return false;
             if (ptx::globaltimer_ns() - t0 > limit_ns) {
                 atomicOr(ab.status, kStatusTimeout | (site << 8));
