@@ -294,6 +294,13 @@ const char *fa_status_string(fa_status s);
  * device-side status word.  Returns FA_ERR_TIMEOUT if a kernel of this
  * library gave up a bounded wait since the last call (its output is then
  * undefined), FA_ERR_CUDA if synchronising failed, FA_OK otherwise.
+ *
+ * Every wait of the tensor-core kernels on another part of the same CTA
+ * gives up after a budget: 4 s by default, or the environment variable
+ * FA_WAIT_LIMIT_MS (milliseconds, fractions allowed), read once per process.
+ * A kernel that gives up still waits, with a budget of at least 1 s, for the
+ * copies and MMAs it has in flight before it exits, so the CUDA context stays
+ * usable.
  */
 fa_status fa_device_status(void *stream);
 
