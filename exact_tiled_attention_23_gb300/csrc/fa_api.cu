@@ -159,9 +159,22 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, in
     return encode_map16(m, base, BH, N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-// Shared checks and launch of the single-pass tensor-core kernel.
+// Query tiles per CTA of the kernel the tensor-core forward runs for a
+// problem: the two-tile kernel's work item covers 256 query rows of one head;
+// the one-tile kernel's covers 128 and runs D = 256, and grids whose twice as
+// many one-tile CTAs still fit in one wave (one CTA per SM).
+int choose_tiles(int B, int H, int N, int D)
+{
+    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    const int forced = forced_tiles();
+    return (D == 256 || forced == 1 || (forced == 0 && 2 * items <= sm_count())) ? 1 : 2;
+}
+
+// Shared checks and launch of the single-pass tensor-core kernel.  tiles: the
+// kernel (1 or 2), or 0 for choose_tiles on this call's sizes.
 fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
-                int N, int D, int causal, float scale, const int32_t *kv_len, void *stream, bool f16)
+                int N, int D, int causal, float scale, const int32_t *kv_len, void *stream, bool f16,
+                int tiles = 0)
 {
     fa_status st = check_common(Q, K, V, O, B, H, N, D);
     if (st != FA_OK) return st;
@@ -170,13 +183,11 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
     if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
     if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
-    // The two-tile kernel's work item covers 256 query rows of one head; the
-    // one-tile kernel's covers 128 and runs D = 256, and grids whose twice as
-    // many one-tile CTAs still fit in one wave (one CTA per SM).  The grid is
-    // 1-D.
+    if (tiles == 0) tiles = choose_tiles(B, H, N, D);
+    if ((tiles != 1 && tiles != 2) || (tiles == 2 && D == 256)) return FA_ERR_INVALID_ARG;
+    const bool one_tile = tiles == 1;
+    // The grid is 1-D.
     const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
-    const int forced = forced_tiles();
-    const bool one_tile = D == 256 || forced == 1 || (forced == 0 && 2 * items <= sm_count());
     const int64_t ctas = one_tile ? (int64_t)B * H * (((int64_t)N + 127) / 128) : items;
     if (ctas > INT32_MAX) return FA_ERR_INVALID_ARG;
     const int64_t BH = (int64_t)B * H;
@@ -246,6 +257,19 @@ fa_status bwd16(const void *Q, const void *K, const void *V, const void *O, cons
 }
 
 }  // namespace
+
+namespace fa {
+
+int fwd16_tiles(int B, int H, int N, int D) { return choose_tiles(B, H, N, D); }
+
+fa_status fwd16_with_tiles(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                           int N, int D, int causal, float scale, const int32_t *kv_len, bool f16, int tiles,
+                           void *stream)
+{
+    return fwd16(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream, f16, tiles);
+}
+
+}  // namespace fa
 
 extern "C" {
 

@@ -13,6 +13,7 @@
 // still allocates no device memory; it keeps four streams and a ring of
 // events per device.
 #include "fa.h"
+#include "fa_internal.h"
 
 #include <cuda_runtime.h>
 
@@ -143,6 +144,10 @@ extern "C" fa_status fa_fwd_from_host(const void *Q_host, const void *K_host, co
         if ((x) != cudaSuccess) return FA_ERR_CUDA; \
     } while (0)
 
+    // Every group runs the kernel fa_fwd would run for the whole problem, so
+    // that the result is fa_fwd's exactly (the kernels agree only to rounding).
+    const int tiles = fa::fwd16_tiles(B, H, N, D);
+
     // Earlier work on the caller's stream may still use the buffers.
     FA_TRY(cudaEventRecord(cs->start, user));
     FA_TRY(cudaStreamWaitEvent(cs->h2d, cs->start, 0));
@@ -172,8 +177,7 @@ extern "C" fa_status fa_fwd_from_host(const void *Q_host, const void *K_host, co
             char *od = static_cast<char *>(O_dev) + off;
             float *ld = LSE_dev ? LSE_dev + first * (size_t)N : nullptr;
             const int32_t *kl = kv_len ? kv_len + b : nullptr;
-            st = f16 ? fa_fwd_f16(qd, kd, vd, od, ld, 1, hc, N, D, causal, scale, kl, comp)
-                     : fa_fwd(qd, kd, vd, od, ld, 1, hc, N, D, causal, scale, kl, comp);
+            st = fa::fwd16_with_tiles(qd, kd, vd, od, ld, 1, hc, N, D, causal, scale, kl, f16 != 0, tiles, comp);
             if (st != FA_OK) return st;
             FA_TRY(cudaEventRecord(outv, comp));
             FA_TRY(cudaStreamWaitEvent(cs->d2h, outv, 0));

@@ -2,11 +2,25 @@
 // of the attention library (not part of the public C ABI).
 #pragma once
 
+#include "fa.h"
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
 namespace fa {
+
+// The tensor-core forward's kernel for a problem of these sizes (query tiles
+// per CTA: 1 or 2), as fa_fwd / fa_fwd_f16 choose it.
+int fwd16_tiles(int B, int H, int N, int D);
+
+// fa_fwd (f16: fa_fwd_f16) with the kernel fixed by `tiles` (1 or 2), for
+// callers that split one problem into several launches and want every part
+// computed as one whole call would compute it: the two kernels agree only to
+// rounding, not bit for bit.
+fa_status fwd16_with_tiles(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                           int N, int D, int causal, float scale, const int32_t *kv_len, bool f16, int tiles,
+                           void *stream);
 
 // Device-side status word.  Kernels OR an error code into the low byte and
 // record the site of the first give-up in the upper bits; the host reads and

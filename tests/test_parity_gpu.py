@@ -353,6 +353,25 @@ def test_from_host_matches_device_forward(dtype, groups):
     compare(inp, o_ref, l_ref)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("groups", [0, 3, 16])
+def test_from_host_two_tile_problem_matches_device_forward(groups, dtype, causal):
+    """A problem for which fa_fwd runs the two-tile kernel, while a group of
+    one or a few heads alone would get the one-tile kernel: every group runs
+    the whole problem's kernel, so the result is fa_fwd's exactly."""
+    inp = workloads.make_case(2, 8, 1300, 128, dtype=dtype, causal=causal, seed=groups + 31,
+                              kv_len=[1300, 700])
+    kv = inp.kv_len.cuda()
+    o_ref, l_ref = fa.forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), causal=causal, kv_len=kv)
+    torch.cuda.synchronize()
+    qh, kh, vh = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+    o, lse = fa.forward_from_host(qh, kh, vh, causal=causal, kv_len=kv, groups=groups)
+    assert fa.fa_device_status(None) == fa.FA_OK
+    assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, l_ref.cpu())
+    compare(inp, o_ref, l_ref)
+
+
 def test_from_host_without_lse_and_on_a_side_stream():
     inp = workloads.make_case(1, 4, 513, 128, dtype="bf16", causal=False, seed=21)
     o_ref, _ = fa.forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), causal=False)
