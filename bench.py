@@ -51,6 +51,11 @@ import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak"
 L2_BYTES = 126 << 20
+# MUFU ex2.approx.ftz.f32 results per clock per SM, measured on a GB300 with
+# independent exponentials on every SM sub-partition (about 8 lanes per clock
+# each).  Every visible score takes at least one exponential, so this rate
+# bounds the attention FLOP rate at D=64 and below, beside the tensor roofline.
+EX2_PER_CLK_PER_SM = 31.0
 UNIT = "TFLOP/s"
 FALLBACK_PEAK_TFLOPS = 1900.0   # used only when MEASURED_PEAKS.json is absent
 HOST_LEAD_CYCLES = 400_000      # about 0.2 ms of SM clock: the host's lead on the device
@@ -480,6 +485,15 @@ def run_ours(args, rank, world, local):
         "gpu_launches": args.steps * (3 if args.pass_ == "bwd" else 2 if splits is not None else 1),
         "clocks": clk.summary(),
     }
+    if roofline["bound"] == "tensor":
+        # the exp2 ceiling: exponentials per second x FLOPs of the metric per
+        # visible score (4D forward, 10D backward), at the sampled SM clock
+        mhz = line["clocks"]["sm_mhz"] or float(peaks.get("sm_max_mhz", 2070.0))
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        per_score = (10 if args.pass_ == "bwd" else 4) * D
+        ceiling = EX2_PER_CLK_PER_SM * sms * mhz * 1e6 * per_score / 1e12
+        roofline["exp2_ceiling"] = ceiling
+        roofline["exp2_frac"] = roofline["achieved"] / ceiling
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
