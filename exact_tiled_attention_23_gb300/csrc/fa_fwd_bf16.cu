@@ -64,12 +64,11 @@ struct Layout {
     static constexpr int kChunkBytes = BM * 128;      // one 128 x 64 bf16 box
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kSlots = (D == 64) ? 8 : 4;  // K/V ring depth (K_j, V_j alternate)
-    // Arrival barriers, one per (V_{j-1}, K_j) pair, used round-robin.  Pair m
-    // is armed by its V tile, whose slot frees only after the MMA warp has
-    // waited on pair m - kSlots/2; one barrier more than that distance makes
-    // pair m's barrier the one of pair m - kSlots/2 - 1, already consumed.
-    // (Pairs up to kSlots/2 fill fresh slots and take fresh barriers.)
-    static constexpr int kPairBars = kSlots / 2 + 1;
+    // K/V tiles move in pairs (V_{m-1}, K_m) -- "pair m"; K_0 alone is pair
+    // 0 and V of the last block alone the last pair.  Pair m fills the slots
+    // of pair m - kPairs, so each pair has one "full" and one "empty"
+    // barrier, used round-robin over kPairs.
+    static constexpr int kPairs = kSlots / 2;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
@@ -82,7 +81,7 @@ struct Layout {
     __device__ static constexpr uint32_t col_o(int i) { return 256u + (uint32_t)i * D; }
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert((1 + kPairBars + kSlots + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((1 + 2 * kPairs + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 
@@ -98,12 +97,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
     uint64_t *q_full = bars;
-    // K/V arrivals are grouped as the MMA warp consumes them: PV(j) reads V_j
-    // and the S(j+1) issued right after it reads K_{j+1}, so one barrier
-    // covers the pair (V_j, K_{j+1}) -- "pair j+1" -- and K_0 alone is pair 0.
-    uint64_t *pair_full = bars + 1;                      // [kPairBars]
-    uint64_t *slot_empty = pair_full + Lay::kPairBars;   // [kSlots]
-    uint64_t *s_full = slot_empty + Lay::kSlots;   // [2]
+    // The MMA warp consumes K/V as pairs: P V_j and the S_{j+1} = Q K_{j+1}^T
+    // issued right after it read (V_j, K_{j+1}) -- pair j+1 -- and the last
+    // products over that pair are issued in the same iteration.  So a pair
+    // arrives together (pair_full) and is released together (pair_empty).
+    uint64_t *pair_full = bars + 1;                   // [kPairs]
+    uint64_t *pair_empty = pair_full + Lay::kPairs;   // [kPairs]
+    uint64_t *s_full = pair_empty + Lay::kPairs;   // [2]
     uint64_t *p_full = s_full + 2;                 // [2]
     uint64_t *o_final = p_full + 2;                // [2]
     uint64_t *mma_drain = o_final + 2;
@@ -139,8 +139,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- set-up -----------------------------------------------------------
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
-        for (int s = 0; s < Lay::kPairBars; ++s) ptx::mbar_init(&pair_full[s], 1);
-        for (int s = 0; s < Lay::kSlots; ++s) ptx::mbar_init(&slot_empty[s], 1);
+        for (int s = 0; s < Lay::kPairs; ++s) {
+            ptx::mbar_init(&pair_full[s], 1);
+            ptx::mbar_init(&pair_empty[s], 1);
+        }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s_full[i], 1);
             ptx::mbar_init(&p_full[i], 4);          // one arrival per softmax warp
@@ -176,45 +178,35 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int c = 0; c < Lay::kChunks; ++c)
                     ptx::tma_load_3d(smem + Lay::kQOff + i * Lay::kTileBytes + c * Lay::kChunkBytes,
                                      &tm_q, q_full, c * 64, (int32_t)(q0 + i * BM), (int32_t)bh);
-            int pairs_armed = 0;    // pairs 0 .. pairs_armed-1 have had tiles issued
-            int open_pair = -1;     // a pair whose first tile went out without its arrival
-            bool ok = true;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                for (int w = 0; w < 2; ++w) {
-                    const int idx = 2 * j + w;
-                    const int slot = idx % Lay::kSlots;
-                    const int round = idx / Lay::kSlots;
-                    if (round > 0 &&
-                        !wait_bounded(&slot_empty[slot], (round - 1) & 1, p.wait_limit_ns,
-                                      kSiteSlotEmpty, ab)) {
-                        ok = false;
+            // Pair m (0 <= m <= n_kv) holds V_{m-1} in slot 2m-1 and K_m in
+            // slot 2m (mod kSlots); from m = kPairs on, those slots are the
+            // ones of pair m - kPairs, which the MMA warp must have released.
+            int pairs_armed = 0;    // pairs 0 .. pairs_armed-1 have had their copies issued
+            for (int m = 0; m <= n_kv; ++m) {
+                if (m >= Lay::kPairs) {
+                    const int pm = m - Lay::kPairs;
+                    if (!wait_bounded(&pair_empty[pm % Lay::kPairs], (pm / Lay::kPairs) & 1, p.wait_limit_ns,
+                                      kSiteSlotEmpty, ab))
                         break;
-                    }
-                    // K_j is pair j (after V_{j-1}); V_j opens pair j+1, which
-                    // K_{j+1} closes -- or V_j alone when it is the last block
-                    const int m = j + w;
-                    uint64_t *bar = &pair_full[m % Lay::kPairBars];
-                    const bool closes = (w == 0) || (j + 1 == n_kv);
-                    if (closes)
-                        ptx::mbar_arrive_expect_tx(bar, Lay::kTileBytes);
-                    else
-                        ptx::mbar_expect_tx(bar, Lay::kTileBytes);
+                }
+                const bool has_v = m >= 1, has_k = m < n_kv;
+                uint64_t *bar = &pair_full[m % Lay::kPairs];
+                ptx::mbar_arrive_expect_tx(bar, (uint32_t)(has_v + has_k) * Lay::kTileBytes);
+                for (int w = has_v ? 1 : 0; w >= (has_k ? 0 : 1); --w) {   // V_{m-1}, then K_m
+                    const int slot = (2 * m - w) % Lay::kSlots;
+                    const int blk = m - w;
                     const CUtensorMap *tm = w ? &tm_v : &tm_k;
                     for (int c = 0; c < Lay::kChunks; ++c)
                         ptx::tma_load_3d(smem + Lay::kKVOff + slot * Lay::kTileBytes + c * Lay::kChunkBytes,
-                                         tm, bar, c * 64, (int32_t)((blk0 + j) * BN), (int32_t)bh);
-                    open_pair = closes ? -1 : m;
-                    pairs_armed = m + 1;
+                                         tm, bar, c * 64, (int32_t)((blk0 + blk) * BN), (int32_t)bh);
                 }
+                pairs_armed = m + 1;
             }
-            // A give-up between the two tiles of a pair: close it, so that its
-            // phase completes once the tile in flight has landed.
-            if (open_pair >= 0) ptx::mbar_arrive(&pair_full[open_pair % Lay::kPairBars]);
             // Drain: no copy may still be landing in shared memory at exit.
             wait_bounded(q_full, 0, p.wait_limit_ns, kSiteDrain, ab, false);
-            for (int m = pairs_armed > Lay::kPairBars ? pairs_armed - Lay::kPairBars : 0; m < pairs_armed; ++m)
-                wait_bounded(&pair_full[m % Lay::kPairBars], (m / Lay::kPairBars) & 1, p.wait_limit_ns,
-                             kSiteDrain, ab, false);
+            for (int m = pairs_armed > Lay::kPairs ? pairs_armed - Lay::kPairs : 0; m < pairs_armed; ++m)
+                wait_bounded(&pair_full[m % Lay::kPairs], (m / Lay::kPairs) & 1, p.wait_limit_ns, kSiteDrain,
+                             ab, false);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
@@ -258,13 +250,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ptx::mma_commit(&s_full[0]);
                 issue_s(1, 0);
                 ptx::mma_commit(&s_full[1]);
-                ptx::mma_commit(&slot_empty[0]);
+                ptx::mma_commit(&pair_empty[0]);      // K_0 is read
             }
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int slot_v = (2 * j + 1) % Lay::kSlots, slot_k = (2 * j + 2) % Lay::kSlots;
                 const bool more = (j + 1 < n_kv);
                 // pair j+1: V_j, and K_{j+1} when there is a next block
-                if (!wait_bounded(&pair_full[(j + 1) % Lay::kPairBars], ((j + 1) / Lay::kPairBars) & 1,
+                if (!wait_bounded(&pair_full[(j + 1) % Lay::kPairs], ((j + 1) / Lay::kPairs) & 1,
                                   p.wait_limit_ns, kSiteSlotFull, ab) ||
                     !wait_bounded(&p_full[0], j & 1, p.wait_limit_ns, kSitePFull, ab))
                     break;
@@ -278,13 +270,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!wait_bounded(&p_full[1], j & 1, p.wait_limit_ns, kSitePFull, ab)) break;
                 ptx::tc_fence_after();
                 issue_pv(1, slot_v, j > 0);
-                ptx::mma_commit(&slot_empty[slot_v]);
                 if (!more) ptx::mma_commit(&o_final[1]);
                 if (more) {
                     issue_s(1, slot_k);
                     ptx::mma_commit(&s_full[1]);
-                    ptx::mma_commit(&slot_empty[slot_k]);
                 }
+                ptx::mma_commit(&pair_empty[(j + 1) % Lay::kPairs]);   // V_j and K_{j+1} are read
             }
             // Drain: every MMA this thread issued is complete before TMEM is
             // freed (on the normal path o_final already covered them; after an

@@ -50,14 +50,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-// Raise the transaction count of the current phase by `bytes`, without an
-// arrival (a later arrive completes the phase once the bytes have landed).
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;"
-                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
 // One non-blocking probe of phase `parity`; true once that phase completed.
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 {
