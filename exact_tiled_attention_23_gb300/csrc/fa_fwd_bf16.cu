@@ -10,7 +10,9 @@
 //     tensor memory (one TMEM lane per query row, fp32);
 //   * warp 0 streams Q once and K_j, V_j through a ring of shared-memory slots
 //     with TMA (128-byte swizzled boxes of 128 rows x 64 columns; a head
-//     dimension below 64 / 128 reads zero-filled columns);
+//     dimension below 64 / 128 reads zero-filled columns).  The tiles move in
+//     the pairs the MMA warp consumes together, (V_j, K_{j+1}): one barrier
+//     signals a pair's arrival and one commit its release;
 //   * warp 1 issues every tcgen05.mma: S_i = Q_i K_j^T (both operands in
 //     shared memory) and O_i += P_i V_j (P_i read from tensor memory);
 //   * warps 4-7 and 8-11 run the online softmax of tile 0 and tile 1: each
