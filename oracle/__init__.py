@@ -19,7 +19,11 @@ Two independent implementations live here:
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (library special cases, closed forms, invariants, Decimal brute force, the
-tiled mirror, planted mutants).  The one item of the pages that cannot be
+tiled mirror, planted mutants).  ``attention_rows()`` has pins of its own for
+the steps it adds (turning a flat row index into batch, head and position,
+and picking that batch's key length): its rows against torch's fp64 softmax
+at the decoded position and, bit for bit, against the same rows of
+``attention()``, with slips planted in that decoding caught.  The one item of the pages that cannot be
 pinned -- the "hand-computed case" of
 "js-flash-attention-tiled-online-softmax-exactness" (Verification), which
 prints outputs but no inputs -- is not used anywhere: parity unpinned.

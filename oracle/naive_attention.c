@@ -91,7 +91,9 @@ static int64_t key_length(const int32_t *kv_len, int64_t b, int64_t N)
 }
 
 /*
- * Selected rows.  rows[r] is the flat row index (b*H + h)*N + i; the outputs
+ * Selected rows: the same definition, for chosen rows only, so that a large
+ * problem can be checked row by row.  rows[r] is the flat row index
+ * (b*H + h)*N + i of batch b, head h, query i; the outputs
  * O_rows [nrows, D] and LSE_rows [nrows] are fp64.  Returns 0, or -1 on a bad
  * argument.  nthreads <= 0 means the OpenMP default.
  */

@@ -18,7 +18,7 @@ import pytest
 import oracle
 from oracle import tiled
 
-from test_oracle_pins import rand, torch_reference
+from test_oracle_pins import ROWS_CASES, boundary_rows, rand, torch_reference
 
 C_MUTANTS = {
     "causal mask drops the diagonal": (
@@ -76,6 +76,86 @@ def test_c_mutant_is_caught(tmp_path, name):
     subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c99", str(mutated),
                     "-o", out, "-lm"], check=True, capture_output=True)
     assert not battery(oracle.OracleLibrary(out)), f"mutant {name!r} survived the pins"
+
+
+# ---- the row-sampled entry point's index decoding ------------------------------
+# oracle_attention_rows shares the per-row step with oracle_attention but turns
+# a flat row index into (batch, head, position) and picks the batch's key
+# length by itself.  Each slip below is planted in that decoding only (the
+# text matched includes names found only there), so the all-rows oracle stays
+# correct and only the rows pins can catch it.  Every planted index stays
+# inside the arrays for the shapes of ROWS_CASES (B*H <= N, H <= B where a
+# key length is read).
+_ROWS_SITE = ("int64_t flat = rows[r];\n"
+              "            int64_t i = flat % N;\n"
+              "            int64_t head = flat / N;\n"
+              "            int64_t b = head / H;\n"
+              "            oracle_row(Q, K, V, N, D, head, i, key_length(kv_len, b, N),\n"
+              "                       causal, scale, s, O_rows + r * D, LSE_rows + r);")
+
+
+def _rows_mutant(old, new):
+    assert old in _ROWS_SITE
+    return _ROWS_SITE, _ROWS_SITE.replace(old, new)
+
+
+ROWS_MUTANTS = {
+    "rows: position from division": _rows_mutant("int64_t i = flat % N;", "int64_t i = flat / N;"),
+    "rows: head drops the batch offset": _rows_mutant("int64_t head = flat / N;",
+                                                      "int64_t head = flat / N % H;"),
+    "rows: batch from head modulo H": _rows_mutant("int64_t b = head / H;", "int64_t b = head % H;"),
+    "rows: key length of batch 0": _rows_mutant("key_length(kv_len, b, N)", "key_length(kv_len, 0, N)"),
+    "rows: key length indexed by head": _rows_mutant("key_length(kv_len, b, N)",
+                                                     "key_length(kv_len, head % B, N)"),
+    "rows: outputs in reversed slots": _rows_mutant("O_rows + r * D", "O_rows + (nrows - 1 - r) * D"),
+}
+
+
+def rows_battery(lib) -> bool:
+    """True when the row-sampled entry point passes its pins: every chosen
+    row equal to torch's fp64 softmax at the decoded (b, h, i) and, bit for
+    bit, to the all-rows oracle."""
+    try:
+        for (B, H, N, D, causal, kv_len, seed) in ROWS_CASES:
+            q, k, v = rand(B, H, N, D, seed)
+            scale = 1.0 / math.sqrt(D)
+            rows = np.array(boundary_rows(B, H, N), dtype=np.int64)
+            o_rows, lse_rows = lib.attention_rows(q, k, v, rows, causal=causal, scale=scale, kv_len=kv_len)
+            ro, rlse, nonempty = torch_reference(q, k, v, causal, scale, kv_len)
+            b, h, i = rows // (H * N), (rows // N) % H, rows % N
+            live = nonempty[b, h, i]
+            if not np.allclose(o_rows[live], ro[b, h, i][live], rtol=0, atol=1e-12):
+                return False
+            if not np.allclose(lse_rows[live], rlse[b, h, i][live], rtol=0, atol=1e-12):
+                return False
+            if not (np.all(o_rows[~live] == 0.0) and np.all(np.isneginf(lse_rows[~live]))):
+                return False
+            o_all, lse_all = lib.attention(q, k, v, causal=causal, scale=scale, kv_len=kv_len)
+            if not (np.array_equal(o_rows, o_all.reshape(-1, D)[rows]) and
+                    np.array_equal(lse_rows, lse_all.reshape(-1)[rows])):
+                return False
+        return True
+    except Exception:
+        return False
+
+
+def test_rows_battery_passes_on_the_real_oracle(oracle_lib):
+    assert rows_battery(oracle_lib)
+
+
+@pytest.mark.parametrize("name", sorted(ROWS_MUTANTS))
+def test_rows_mutant_is_caught(tmp_path, name):
+    old, new = ROWS_MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation site for {name!r} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    out = str(tmp_path / "libmutant.so")
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c99", str(mutated),
+                    "-o", out, "-lm"], check=True, capture_output=True)
+    lib = oracle.OracleLibrary(out)
+    assert battery(lib), f"mutant {name!r} also broke the all-rows oracle"
+    assert not rows_battery(lib), f"mutant {name!r} survived the rows pins"
 
 
 # ---- the tiled mirror's update step --------------------------------------------

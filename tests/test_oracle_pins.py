@@ -414,3 +414,84 @@ def test_merge_identity_and_empty_sides():
     m2 = tiled.merge(masked, st)
     np.testing.assert_allclose(m2.acc, st.acc, atol=0)
     del rng
+
+
+# ------------------------------------------------- the row-sampled oracle
+# oracle_attention_rows computes chosen rows of the same definition, one flat
+# row index r = (b*H + h)*N + i at a time.  It decodes (b, h, i) and picks the
+# batch's key length on its own, so its pin checks exactly those steps: each
+# chosen row against torch's fp64 softmax on the same (b, h, i) (a library
+# routine, independent of the C code), and bit for bit against the same row
+# of the all-rows oracle.  The shapes have B, H >= 3, N not a power of two and
+# key lengths of 0, 1, N, a ragged value and values outside [0, N], so a row
+# decoded to the wrong batch, head or position, or given another batch's key
+# length, lands on different data.
+ROWS_CASES = [
+    # B, H, N, D, causal, kv_len, seed
+    (3, 3, 37, 8, True, [0, 37, 20], 61),
+    (4, 3, 45, 6, False, [1, 45, 0, 60], 62),
+    (3, 2, 50, 5, True, [-3, 50, 17], 63),
+    (3, 4, 29, 12, False, None, 64),
+    (5, 3, 33, 16, True, [33, 1, 9, 0, 32], 65),
+]
+
+
+def boundary_rows(B, H, N):
+    """Flat rows at the first and last position of every head, plus the rows
+    next to each batch boundary."""
+    rows = set()
+    for b in range(B):
+        for h in range(H):
+            base = (b * H + h) * N
+            rows.update({base, base + 1, base + N // 2, base + N - 2, base + N - 1})
+    return sorted(r for r in rows if 0 <= r < B * H * N)
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,kv_len,seed", ROWS_CASES)
+def test_attention_rows_match_torch_and_all_rows(oracle_lib, B, H, N, D, causal, kv_len, seed):
+    q, k, v = rand(B, H, N, D, seed)
+    scale = 1.0 / math.sqrt(D)
+    rng = np.random.default_rng(seed)
+    rows = np.array(boundary_rows(B, H, N) + rng.integers(0, B * H * N, 64).tolist(), dtype=np.int64)
+    o_rows, lse_rows = oracle_lib.attention_rows(q, k, v, rows, causal=causal, scale=scale, kv_len=kv_len)
+    assert o_rows.shape == (rows.size, D) and lse_rows.shape == (rows.size,)
+
+    # independent: torch fp64 softmax at the (b, h, i) each row decodes to
+    ro, rlse, nonempty = torch_reference(q, k, v, causal, scale, kv_len)
+    b, h, i = rows // (H * N), (rows // N) % H, rows % N
+    live = nonempty[b, h, i]
+    np.testing.assert_allclose(o_rows[live], ro[b, h, i][live], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse_rows[live], rlse[b, h, i][live], rtol=1e-13, atol=1e-13)
+    assert np.all(o_rows[~live] == 0.0) and not np.any(np.signbit(o_rows[~live]))
+    assert np.all(np.isneginf(lse_rows[~live]))
+
+    # the same rows of the all-rows oracle, bit for bit
+    o_all, lse_all = oracle_lib.attention(q, k, v, causal=causal, scale=scale, kv_len=kv_len)
+    np.testing.assert_array_equal(o_rows, o_all.reshape(-1, D)[rows])
+    np.testing.assert_array_equal(lse_rows, lse_all.reshape(-1)[rows])
+
+
+def test_attention_rows_every_row_in_order_and_shuffled(oracle_lib):
+    """All rows requested, in order and shuffled with repeats: the result
+    follows the request order exactly."""
+    B, H, N, D = 3, 3, 19, 4
+    q, k, v = rand(B, H, N, D, 66)
+    kv = [19, 0, 7]
+    o_all, lse_all = oracle_lib.attention(q, k, v, causal=True, kv_len=kv)
+    rows = np.arange(B * H * N)
+    o_rows, lse_rows = oracle_lib.attention_rows(q, k, v, rows, causal=True, kv_len=kv)
+    np.testing.assert_array_equal(o_rows, o_all.reshape(-1, D))
+    np.testing.assert_array_equal(lse_rows, lse_all.reshape(-1))
+    perm = np.random.default_rng(1).permutation(np.concatenate([rows, rows[:10]]))
+    o_p, lse_p = oracle_lib.attention_rows(q, k, v, perm, causal=True, kv_len=kv)
+    np.testing.assert_array_equal(o_p, o_all.reshape(-1, D)[perm])
+    np.testing.assert_array_equal(lse_p, lse_all.reshape(-1)[perm])
+
+
+def test_attention_rows_rejects_out_of_range_rows(oracle_lib):
+    q, k, v = rand(2, 2, 5, 4, 67)
+    for bad in ([-1], [2 * 2 * 5]):
+        with pytest.raises(RuntimeError):
+            oracle_lib.attention_rows(q, k, v, bad, causal=True)
+    o, lse = oracle_lib.attention_rows(q, k, v, [], causal=True)
+    assert o.shape == (0, 4) and lse.shape == (0,)
