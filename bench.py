@@ -18,8 +18,9 @@ Also reported on the same line:
                 the next);
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the same
                 workload on this host's cores (rank 0, N=1 only);
-  clocks        nvidia-smi SM clocks and throttle reasons sampled during the
-                timed region.
+  clocks        SM clocks, power and throttle reasons sampled (NVML, read
+                only) every 2 ms during the timed region, and SM cycles per
+                step at the median clock.
 
 --impl reference times the CPU oracle alone (the reference arm).
 Multi-GPU: one process per GPU under torchrun; the path shards by
@@ -118,62 +119,127 @@ def profiled_traffic(workload: str, kernel: str):
     return ent.get("dram_bytes_per_launch")
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (clocks, power, clock-event
+    reasons).  Nothing here changes a GPU setting."""
+
+    # clock-event reason bits of nvml.h
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.max_mhz = self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        if fn(self.dev, self.ct.c_int(1), self.ct.byref(v)) != 0:    # NVML_CLOCK_SM
+            raise OSError("clock query failed")
+        return float(v.value)
+
+    def sample(self):
+        sm = self._clock(self.lib.nvmlDeviceGetClockInfo)
+        bits = self.ct.c_ulonglong()
+        self.reasons_fn(self.dev, self.ct.byref(bits))
+        mw = self.ct.c_uint()
+        self.lib.nvmlDeviceGetPowerUsage(self.dev, self.ct.byref(mw))
+        reasons = [n for b, n in self.REASONS.items() if bits.value & b]
+        return sm, self.max_mhz, mw.value / 1e3, reasons
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed loop runs."""
+    """SM clock, power and clock-event reasons sampled every few milliseconds
+    while the timed loop runs: NVML through ctypes in a thread (every 2 ms),
+    else nvidia-smi (every 10 ms).  Entering waits for the first sample, so
+    even a region of a few tens of milliseconds carries several."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.thread = None
+        self.samples = []            # (sm_mhz, max_mhz, watts, [reasons])
+        self.source = "none"
+        self._stop = threading.Event()
+        self._first = threading.Event()
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            nv = _Nvml(self.gpu)
+            nv.sample()
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll_nvml, args=(nv,), daemon=True)
+        except (OSError, AttributeError):
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                     "--format=csv,noheader,nounits", "-lms", "10"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                self.thread = threading.Thread(target=self._read_smi, daemon=True)
+            except OSError:
+                self.proc = None
+        if self.thread is not None:
             self.thread.start()
-        except OSError:
-            self.proc = None
+            self._first.wait(timeout=5.0)
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _poll_nvml(self, nv):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.sample())
+            except OSError:
+                pass
+            self._first.set()
+            time.sleep(self.PERIOD_S)
+
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.proc.stdout:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+                watts = float(parts[3]) if parts[3] not in ("", "[N/A]") else float("nan")
+            except ValueError:
+                continue
+            self.samples.append((sm, mx, watts, [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]))
+            self._first.set()
 
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        sm = [x[0] for x in self.samples]
+        watts = [x[2] for x in self.samples if x[2] == x[2]]
+        reasons = sorted({r for x in self.samples for r in x[3]})
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(x[1] for x in self.samples),
+                "power_w_max": max(watts) if watts else None, "reasons": reasons,
+                "samples": len(sm), "source": self.source}
 
 
 # ------------------------------------------------------------ multi-rank
@@ -485,6 +551,10 @@ def run_ours(args, rank, world, local):
         "gpu_launches": args.steps * (3 if args.pass_ == "bwd" else 2 if splits is not None else 1),
         "clocks": clk.summary(),
     }
+    if line["clocks"]["sm_mhz"]:
+        # SM cycles per step at the sampled median clock: comparable across
+        # boxes whose clocks differ
+        line["clocks"]["kcycles_per_step"] = t_max / args.steps * 1e-3 * line["clocks"]["sm_mhz"] * 1e3
     if roofline["bound"] == "tensor":
         # the exp2 ceiling: exponentials per second x FLOPs of the metric per
         # visible score (4D forward, 10D backward), at the sampled SM clock

@@ -18,7 +18,6 @@ other code path, and calling without the built library raises.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 
@@ -265,10 +264,6 @@ def forward(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse
     if st != FA_OK:
         raise FAError(st, fn.__name__)
     return (out, lse) if return_lse else out
-
-
-def default_scale(D: int) -> float:
-    return 1.0 / math.sqrt(D)
 
 
 def forward_from_host(q, k, v, causal: bool = True, scale=None, kv_len=None, out=None, lse=None,

@@ -330,9 +330,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&p_full[i]);
         }
-        const float l = st.l, m_ref = st.m_ref;
+        const float l = st.l, l_o = st.l_o, m_ref = st.m_ref;
 
-        // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----------------
+        // ---- epilogue: O = acc / l_o, LSE = (m + log2 l) ln 2 --------------
         bool have = (n_kv > 0) && ok;
         if (have) have = wait_bounded(&o_final[i], 0, p.wait_limit_ns, kSiteOFinal, ab);
         // the tile's four warps agree, so that its named barrier below is
@@ -341,7 +341,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (have || n_kv == 0) {
             ptx::tc_fence_after();
             const bool empty = !(l > 0.f);
-            const float inv = empty ? 0.f : 1.f / l;
+            const float inv = empty ? 0.f : 1.f / l_o;      // O / (sum of the P the MMA used)
             const float lse_row = empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
             // Only the first p.D (a multiple of 8, <= D) columns exist in
             // memory; the rest of the D computed ones are the zero padding.
@@ -375,7 +375,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 }
             } else {
-                // O = acc / l as 16-bit, staged in this tile's Q buffer (free:
+                // O = acc / l_o as 16-bit, staged in this tile's Q buffer (free:
                 // every MMA has completed) as 128-byte-swizzled 128 x 64 boxes,
                 // then written by TMA stores that clip rows >= N and columns
                 // >= p.D.

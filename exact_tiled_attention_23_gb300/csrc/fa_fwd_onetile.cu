@@ -4,22 +4,28 @@
 // The computation is the tiled online-softmax forward of "vectorized-flash-
 // attention-kernel" (Core algorithm; Key design decisions 1-3), with the same
 // per-row softmax step as the two-tile kernel (fa_fwd_softmax.cuh).  Only the
-// layout on the SM differs.  It serves head dimension 256, whose output tile
-// takes 256 of the 512 TMEM columns, and grids where the two-tile kernel's
-// 256-row items would not fill the GPU (twice as many CTAs):
+// layout on the SM differs:
 //
 //   * one CTA owns one 128-row query tile; TMEM holds two score tiles S_a,
-//     S_b (128 columns each) and O (D columns);
-//   * warp 1 issues S_{j+1} = Q K_{j+1}^T into the other score tile before
-//     O += P_j V_j, so the tensor core computes the next block's scores while
-//     warps 4-7 run the softmax of this one;
-//   * shared memory holds Q and one K and one V tile (D x 256 bytes each);
-//     warp 0 loads K_{j+1} as soon as S_j has consumed K_j, ahead of V_j,
-//     which waits for O += P_{j-1} V_{j-1}.
+//     S_b (128 columns each), O (D columns) and, for D <= 128, two P tiles of
+//     their own (64 columns each: 16-bit pairs);
+//   * warp 1 issues the MMAs in the order S_0, S_1, then per key block j:
+//     O += P_j V_j and S_{j+2} = Q K_{j+2}^T into the score tile S_j has
+//     left.  The tensor core so holds the next block's scores ready while
+//     warps 4-7 run the softmax of this one, and the softmax never waits for
+//     the products that follow it: with P apart from S, S_{j+2} may be
+//     computed as soon as the softmax of block j has read S_j;
+//   * warp 0 streams K and V through rings of kRing slots each, in the order
+//     the MMAs read them (K_0, K_1, V_0, K_2, V_1, ...), so a load has several
+//     blocks' time to land;
+//   * at D = 256 the output tile takes 256 TMEM columns, so P is written over
+//     the first 64 columns of its score tile and K, V have one slot each.
 //
 // O is rescaled in TMEM only when the lazy reference max moves; because
 // O += P_{j-1} V_{j-1} may still be running when the softmax of block j
-// starts, such a rescale first waits for that product (pv_done).
+// starts, such a rescale first waits for that product.  P tile j % 2 is free
+// for block j once S_j is complete: S_j is issued after O += P_{j-2} V_{j-2},
+// the last reader of that tile, and its commit covers every earlier MMA.
 //
 // Every mbarrier wait is bounded; a wait that runs out records the site in
 // this file's status word, raises the CTA's abort flag, and every role drains
@@ -49,15 +55,27 @@ template <int D>
 struct OneTileLayout {
     static constexpr int kChunks = D / 64;                  // 128-byte swizzle atoms per row
     static constexpr int kTileBytes = kChunks * kChunkBytes;    // Q, a K or a V tile
+    // K and V slots each: as many as shared memory holds next to Q
+    static constexpr int kRing = D == 256 ? 1 : (D == 128 ? 3 : 4);
+    // P in TMEM columns of its own (two tiles of 64) where O leaves room
+    static constexpr bool kPApart = D <= 128;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kTileBytes;
-    static constexpr int kVOff = 2 * kTileBytes;
-    static constexpr int kBarOff = 3 * kTileBytes;
+    static constexpr int kKOff = kTileBytes;                        // K slots
+    static constexpr int kVOff = kKOff + kRing * kTileBytes;        // V slots
+    static constexpr int kBarOff = kVOff + kRing * kTileBytes;
+    static constexpr int kBars = 1 + 4 * kRing + 9;
     // At least 120 KB, so that one CTA (and its 512 TMEM columns) sits on an SM.
     static constexpr int kNeed = kBarOff + 256 + 1024;      // + alignment slack
     static constexpr int kSmemBytes = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
+    // TMEM column of P tile `buf`
+    __device__ static constexpr uint32_t col_p(int buf)
+    {
+        return kPApart ? kColO + (uint32_t)D + (uint32_t)buf * 64u : (uint32_t)buf * 128u;
+    }
     static_assert(D == 64 || D == 128 || D == 256, "head dim");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kBars * 8 + 8 <= 256, "barrier area");
+    static_assert(!kPApart || kColO + D + 128 <= kTmemCols, "TMEM columns");
 };
 
 __device__ __forceinline__ uint32_t col_s(int buf) { return (uint32_t)buf * 128u; }
@@ -69,23 +87,23 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const FwdParams p, const int q_tiles)
 {
     using Lay = OneTileLayout<D>;
-    constexpr int kChunks = Lay::kChunks, kTileBytes = Lay::kTileBytes;
+    constexpr int kChunks = Lay::kChunks, kTileBytes = Lay::kTileBytes, R = Lay::kRing;
     constexpr int kQOff = Lay::kQOff, kKOff = Lay::kKOff, kVOff = Lay::kVOff;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
     uint64_t *q_full = bars + 0;
-    uint64_t *k_full = bars + 1;
-    uint64_t *k_empty = bars + 2;
-    uint64_t *v_full = bars + 3;
-    uint64_t *v_empty = bars + 4;
-    uint64_t *s_full = bars + 5;     // [2], per score tile
-    uint64_t *p_full = bars + 7;     // [2], per score tile
-    uint64_t *pv_done = bars + 9;    // one phase per O += P V
-    uint64_t *o_final = bars + 10;
-    uint64_t *mma_drain = bars + 11;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *k_full = bars + 1;               // [R]
+    uint64_t *k_empty = k_full + R;            // [R]
+    uint64_t *v_full = k_empty + R;            // [R]
+    uint64_t *v_empty = v_full + R;            // [R]
+    uint64_t *s_full = v_empty + R;            // [2], per score tile
+    uint64_t *p_full = s_full + 2;             // [2], per P tile
+    uint64_t *pv_done = p_full + 2;            // [2], per P tile: O += P V has read it
+    uint64_t *o_final = pv_done + 2;
+    uint64_t *mma_drain = o_final + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Lay::kBars);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     const Abort ab{abort_word, &g_status_onetile};
 
@@ -108,7 +126,8 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int n_kv = (int)((kv_end + BN - 1) / BN);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 12; ++i)   // p_full: one arrival per softmax warp; the rest: one
+        // P hand-offs take one arrival per softmax warp, the rest one
+        for (int i = 0; i < Lay::kBars; ++i)
             ptx::mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? 4 : 1);
         *abort_word = 0;
         ptx::fence_mbarrier_init();
@@ -134,32 +153,40 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ptx::tma_load_3d(smem + off + c * kChunkBytes, tm, bar, c * 64, (int32_t)row0, (int32_t)bh);
             };
             load_tile(&tm_q, kQOff, q_full, q0);
-            load_tile(&tm_k, kKOff, k_full, 0);
-            load_tile(&tm_v, kVOff, v_full, 0);
-            // K_t (t >= 1) waits until S_{t-1} has read K_{t-1}; V_t waits
-            // until O += P_{t-1} V_{t-1} is done.  The MMA order (S_{j+1}
-            // before P_j V_j) frees K first, so K_{j+1} goes before V_j.
-            int k_issued = 1, v_issued = 1;
-            bool ok = true;
-            if (n_kv > 1) {
-                ok = wait_bounded(k_empty, 0, p.wait_limit_ns, kSiteSlotEmpty, ab);
-                if (ok) load_tile(&tm_k, kKOff, k_full, (int64_t)BN);
-                k_issued += ok ? 1 : 0;
-            }
-            for (int j = 1; j < n_kv && ok; ++j) {
-                if (j + 1 < n_kv) {
-                    if (!wait_bounded(k_empty, j & 1, p.wait_limit_ns, kSiteSlotEmpty, ab)) break;
-                    load_tile(&tm_k, kKOff, k_full, (int64_t)(j + 1) * BN);
-                    ++k_issued;
-                }
-                if (!wait_bounded(v_empty, (j - 1) & 1, p.wait_limit_ns, kSiteSlotEmpty, ab)) break;
-                load_tile(&tm_v, kVOff, v_full, (int64_t)j * BN);
+            // Loads in the order the MMAs read them: K_0, K_1, then V_t and
+            // K_{t+2} in turn.  K_t goes into slot t % R once S_{t-R} has read
+            // that slot, V_t once O += P_{t-R} V_{t-R} has.
+            int k_issued = 0, v_issued = 0;
+            auto load_k = [&]() -> bool {
+                const int t = k_issued;
+                if (t >= R &&
+                    !wait_bounded(&k_empty[t % R], ((t - R) / R) & 1, p.wait_limit_ns, kSiteSlotEmpty, ab))
+                    return false;
+                load_tile(&tm_k, kKOff + (t % R) * kTileBytes, &k_full[t % R], (int64_t)t * BN);
+                ++k_issued;
+                return true;
+            };
+            auto load_v = [&]() -> bool {
+                const int t = v_issued;
+                if (t >= R &&
+                    !wait_bounded(&v_empty[t % R], ((t - R) / R) & 1, p.wait_limit_ns, kSiteSlotEmpty, ab))
+                    return false;
+                load_tile(&tm_v, kVOff + (t % R) * kTileBytes, &v_full[t % R], (int64_t)t * BN);
                 ++v_issued;
+                return true;
+            };
+            bool ok = load_k();
+            if (ok && n_kv > 1) ok = load_k();
+            while (ok && v_issued < n_kv) {
+                ok = load_v();
+                if (ok && k_issued < n_kv) ok = load_k();
             }
             // Drain: no copy may still be landing in shared memory at exit.
             wait_bounded(q_full, 0, p.wait_limit_ns, kSiteDrain, ab, false);
-            wait_bounded(k_full, (k_issued - 1) & 1, p.wait_limit_ns, kSiteDrain, ab, false);
-            wait_bounded(v_full, (v_issued - 1) & 1, p.wait_limit_ns, kSiteDrain, ab, false);
+            for (int t = k_issued > R ? k_issued - R : 0; t < k_issued; ++t)
+                wait_bounded(&k_full[t % R], (t / R) & 1, p.wait_limit_ns, kSiteDrain, ab, false);
+            for (int t = v_issued > R ? v_issued - R : 0; t < v_issued; ++t)
+                wait_bounded(&v_full[t % R], (t / R) & 1, p.wait_limit_ns, kSiteDrain, ab, false);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
@@ -171,47 +198,54 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint32_t va = ptx::smem_u32(smem + kVOff);
             // The start-address field of a descriptor is the byte address / 16,
             // and every operand lies below 256 KiB: the descriptors are built
-            // once, and each K-step adds its byte offset / 16.
+            // once, and each slot and K-step adds its byte offset / 16.
             const uint64_t q_desc = make_sdesc(qa, 16, 1024);
             const uint64_t k_desc = make_sdesc(ka, 16, 1024);
             const uint64_t v_desc = make_sdesc(va, kChunkBytes, 1024);
-            auto issue_s = [&](int buf) {
+            constexpr uint64_t kTileStep = kTileBytes >> 4;
+            auto issue_s = [&](int buf, int slot) {
+                const uint64_t kd = k_desc + (uint64_t)slot * kTileStep;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t off = (uint64_t)(((k / 4) * kChunkBytes + (k % 4) * 32) >> 4);
-                    ptx::mma_ss(tmem + col_s(buf), q_desc + off, k_desc + off, idesc_qk, k > 0);
+                    ptx::mma_ss(tmem + col_s(buf), q_desc + off, kd + off, idesc_qk, k > 0);
                 }
             };
-            auto issue_pv = [&](int buf, bool acc) {
+            auto issue_pv = [&](int buf, int slot, bool acc) {
+                const uint64_t vd = v_desc + (uint64_t)slot * kTileStep;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                    ptx::mma_ts(tmem + kColO, tmem + col_s(buf) + k * 8, v_desc + (uint64_t)((k * 2048) >> 4),
+                    ptx::mma_ts(tmem + kColO, tmem + Lay::col_p(buf) + k * 8, vd + (uint64_t)((k * 2048) >> 4),
                                 idesc_pv, acc || k > 0);
             };
-            bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
-                      wait_bounded(k_full, 0, p.wait_limit_ns, kSiteSlotFull, ab);
-            if (ok) {
+            // S_t into score tile t % 2 (K_t in slot t % R)
+            auto next_s = [&](int t) -> bool {
+                if (!wait_bounded(&k_full[t % R], (t / R) & 1, p.wait_limit_ns, kSiteSlotFull, ab)) return false;
                 ptx::tc_fence_after();
-                issue_s(0);
-                ptx::mma_commit(&s_full[0]);
-                ptx::mma_commit(k_empty);
-            }
+                issue_s(t & 1, t % R);
+                ptx::mma_commit(&s_full[t & 1]);
+                ptx::mma_commit(&k_empty[t % R]);
+                return true;
+            };
+            bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) && next_s(0);
+            // P apart from S: both score tiles are free at the start.
+            if (ok && Lay::kPApart && n_kv > 1) ok = next_s(1);
             for (int j = 0; j < n_kv && ok; ++j) {
-                if (j + 1 < n_kv) {
-                    if (!wait_bounded(k_full, (j + 1) & 1, p.wait_limit_ns, kSiteSlotFull, ab)) break;
-                    ptx::tc_fence_after();
-                    issue_s((j + 1) & 1);
-                    ptx::mma_commit(&s_full[(j + 1) & 1]);
-                    ptx::mma_commit(k_empty);
-                }
-                if (!wait_bounded(v_full, j & 1, p.wait_limit_ns, kSiteSlotFull, ab) ||
-                    !wait_bounded(&p_full[j & 1], (j >> 1) & 1, p.wait_limit_ns, kSitePFull, ab))
+                const int buf = j & 1;
+                // P over S: S_{j+1} goes into the score tile P_{j-1} has left,
+                // after O += P_{j-1} V_{j-1} (issued before it, so read before).
+                if (!Lay::kPApart && j + 1 < n_kv && !next_s(j + 1)) break;
+                if (!wait_bounded(&v_full[j % R], (j / R) & 1, p.wait_limit_ns, kSiteSlotFull, ab) ||
+                    !wait_bounded(&p_full[buf], (j >> 1) & 1, p.wait_limit_ns, kSitePFull, ab))
                     break;
                 ptx::tc_fence_after();
-                issue_pv(j & 1, j > 0);
-                ptx::mma_commit(v_empty);
-                ptx::mma_commit(pv_done);
+                issue_pv(buf, j % R, j > 0);
+                ptx::mma_commit(&v_empty[j % R]);
+                ptx::mma_commit(&pv_done[buf]);
                 if (j + 1 == n_kv) ptx::mma_commit(o_final);
+                // P apart: S_{j+2} into the score tile the softmax of block j
+                // has read (it handed P_j over after reading S_j).
+                if (Lay::kPApart && j + 2 < n_kv && !next_s(j + 2)) break;
             }
             // Drain: every MMA issued here completes before TMEM is freed.
             ptx::mma_commit(mma_drain);
@@ -232,11 +266,15 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int j = 0; j < n_kv; ++j) {
             const int buf = j & 1;
             const uint32_t tS = tmem + lane_off + col_s(buf);
+            const uint32_t tP = tmem + lane_off + Lay::col_p(buf);
             const bool got = wait_bounded(&s_full[buf], (j >> 1) & 1, p.wait_limit_ns, kSiteSFull, ab);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
+            // P tile `buf` was last read by O += P_{j-2} V_{j-2}.  S_j was
+            // issued after that product, and the commit that completed S_j
+            // covers every earlier op of the MMA thread, so the tile is free.
             ptx::tc_fence_after();
             uint32_t s_raw[4][32];
 #pragma unroll
@@ -253,8 +291,8 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // O += P_{j-1} V_{j-1} may still be running: an O rescale waits
             // for it first.
             bool hook_ok = true;
-            st.block(s_raw, sl2, j > 0, tS, tO, [&] {
-                hook_ok = wait_bounded(pv_done, (j - 1) & 1, p.wait_limit_ns, kSiteOFinal, ab);
+            st.block(s_raw, sl2, j > 0, tP, tO, [&] {
+                hook_ok = wait_bounded(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.wait_limit_ns, kSiteOFinal, ab);
                 ptx::tc_fence_after();
             });
             // every lane's P stores have landed; after the warp has
@@ -268,7 +306,7 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
 
-        // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2 ----------------
+        // ---- epilogue: O = acc / l_o, LSE = (m + log2 l) ln 2 --------------
         bool have = (n_kv > 0) && ok;
         if (have) have = wait_bounded(o_final, 0, p.wait_limit_ns, kSiteOFinal, ab);
         // the four softmax warps agree, so that the named barrier below is
@@ -277,14 +315,14 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (have || n_kv == 0) {
             ptx::tc_fence_after();
             const bool empty = !(st.l > 0.f);
-            const float inv = empty ? 0.f : 1.f / st.l;
+            const float inv = empty ? 0.f : 1.f / st.l_o;   // O / (sum of the P the MMA used)
             const float lse_row = empty ? -INFINITY : (st.m_ref + log2f(st.l)) * 0.69314718055994530942f;
             // Only the first p.D (a multiple of 8, <= D) columns exist in
             // memory; the rest of the D computed ones are the zero padding.
             const int Dv = (int)p.D;
             const int64_t flat = bh * N + row;
             (void)Dv;
-            // O = acc / l as 16-bit, staged in the Q buffer (free: every MMA
+            // O = acc / l_o as 16-bit, staged in the Q buffer (free: every MMA
             // has completed) as 128-byte-swizzled 128 x 64 boxes, then written
             // by TMA stores that clip rows >= N and columns >= p.D.
             uint8_t *obuf = smem + kQOff;

@@ -4,10 +4,19 @@
 // One thread owns one query row (one TMEM lane).  Per key block it has the
 // row's 128 raw scores S = q.k in registers (fp32 bits, masked entries
 // already -inf) and turns them into P = 2^(S*scale*log2e - m_ref), stored as
-// 16-bit pairs over the first 64 TMEM columns of the score tile, while
-// keeping the running sum l against the same reference m_ref.  This is the
+// 16-bit pairs in 64 TMEM columns (over the first 64 columns of the score
+// tile, or in columns of their own), while keeping the running sum l against
+// the same reference m_ref.  This is the
 // recurrence of "vectorized-flash-attention-kernel", Core algorithm step 3,
 // in base 2.
+//
+// Two running sums are kept.  l sums the fp32 p and gives the LSE.  l_o sums
+// the same p after rounding to the 16-bit type, i.e. exactly the weights the
+// tensor core multiplies V by, and normalises O: O = sum(P~ V) / sum(P~) is a
+// convex combination of V rows whatever the rounding, so a dominant weight's
+// rounding error cancels.  With the lazy reference below the dominant p is
+// not 1, and normalising by the fp32 sum instead leaves its relative rounding
+// error (up to 2^-8 for bf16) on O: 2.6e-2 on |O| ~ 4 in near one-hot rows.
 //
 // The reference max is lazy.  The first key block sets it from the row max.
 // Later blocks reuse it without scanning for their max as long as the block's
@@ -37,7 +46,8 @@ constexpr float kLazyLimitF16 = 32768.f;
 template <int D, bool kF16>
 struct OnlineRow {
     float m_ref = -INFINITY;   // reference max of scale*log2e*S: a lower bound of the running max
-    float l = 0.f;             // running sum of p against m_ref
+    float l = 0.f;             // running sum of p against m_ref (fp32 p): the LSE
+    float l_o = 0.f;           // running sum of the 16-bit rounded P: O's normaliser
 
     // Raise m_ref to the block's max; rescale l (and O in TMEM at tO when it
     // already holds earlier blocks) by 2^(m_old - m_new).  before_o_touch()
@@ -67,34 +77,39 @@ struct OnlineRow {
             before_o_touch();
             const uint64_t a2 = ptx::pack2(alpha, alpha);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                ptx::tmem_ld32(tO + c * 32, o);
+            for (int c = 0; c < D / 16; ++c) {       // 16 columns at a time: few registers beside S
+                uint32_t o[16];
+                ptx::tmem_ld16(tO + c * 16, o);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
+                for (int t = 0; t < 8; ++t) {
                     float lo, hi;
                     ptx::unpack2(ptx::mul2(ptx::pack2(u2f(o[2 * t]), u2f(o[2 * t + 1])), a2), lo, hi);
                     o[2 * t] = f2u(lo);
                     o[2 * t + 1] = f2u(hi);
                 }
-                ptx::tmem_st32(tO + c * 32, o);
+                ptx::tmem_st16(tO + c * 16, o);
             }
         }
         l *= alpha;
+        l_o *= alpha;
         m_ref = m_new;
     }
 
     // p = 2^(S*scale*log2e - m_ref): packed FMA, MUFU ex2, packed sums; P
-    // goes to the first 64 columns at tS as 16-bit pairs.  Returns sum p.
-    __device__ __forceinline__ float exp_pass(const uint32_t (&s)[4][32], float sl2, uint32_t tS) const
+    // goes to the 64 columns at tP as 16-bit pairs.  Returns sum p in `sum`
+    // and the sum of the stored (rounded) P in `sum_o`.
+    __device__ __forceinline__ void exp_pass(const uint32_t (&s)[4][32], float sl2, uint32_t tP, float &sum,
+                                             float &sum_o) const
     {
         const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const uint64_t t2 = ptx::pack2(sl2, sl2);
         const uint64_t nm2 = ptx::pack2(-mref_use, -mref_use);
-        uint64_t acc2[4];
+        uint64_t acc2[4], rnd2[2];
 #pragma unroll
         for (int a = 0; a < 4; ++a) acc2[a] = 0ull;
+#pragma unroll
+        for (int a = 0; a < 2; ++a) rnd2[a] = 0ull;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
@@ -106,34 +121,40 @@ struct OnlineRow {
                 const float p1 = ptx::ex2_approx(y1);
                 acc2[t & 3] = ptx::add2(acc2[t & 3], ptx::pack2(p0, p1));
                 pk[t] = ptx::pack16x2<kF16>(p0, p1);
+                rnd2[t & 1] = ptx::add2(rnd2[t & 1], ptx::widen16x2<kF16>(pk[t]));
             }
-            ptx::tmem_st16(tS + c * 16, pk);
+            ptx::tmem_st16(tP + c * 16, pk);
         }
         float a0, a1, b0, b1, c0, c1, d0, d1;
         ptx::unpack2(acc2[0], a0, a1);
         ptx::unpack2(acc2[1], b0, b1);
         ptx::unpack2(acc2[2], c0, c1);
         ptx::unpack2(acc2[3], d0, d1);
-        return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+        sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+        ptx::unpack2(rnd2[0], a0, a1);
+        ptx::unpack2(rnd2[1], b0, b1);
+        sum_o = (a0 + a1) + (b0 + b1);
     }
 
-    // One key block.  o_live: O at tO holds earlier blocks.  before_o_touch()
-    // runs (warp-uniformly) before any access to O, for kernels whose O may
-    // still be written by an MMA at that point.  On return every P store has
-    // landed in TMEM.
+    // One key block; P goes to tP.  o_live: O at tO holds earlier blocks.
+    // before_o_touch() runs (warp-uniformly) before any access to O, for
+    // kernels whose O may still be written by an MMA at that point.  On
+    // return every P store has landed in TMEM.
     template <typename Hook>
-    __device__ __forceinline__ void block(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tS,
+    __device__ __forceinline__ void block(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tP,
                                           uint32_t tO, Hook &&before_o_touch)
     {
         if (__any_sync(0xffffffffu, m_ref == -INFINITY)) raise(s, sl2, o_live, tO, before_o_touch);
-        float sum = exp_pass(s, sl2, tS);
+        float sum, sum_o;
+        exp_pass(s, sl2, tP, sum, sum_o);
         if (__any_sync(0xffffffffu, !(sum <= (kF16 ? kLazyLimitF16 : kLazyLimit)))) {
             raise(s, sl2, o_live, tO, before_o_touch);
             ptx::tmem_wait_st();      // the first pass's P stores land before the new ones
-            sum = exp_pass(s, sl2, tS);
+            exp_pass(s, sl2, tP, sum, sum_o);
         }
         ptx::tmem_wait_st();
         l += sum;
+        l_o += sum_o;
     }
 };
 

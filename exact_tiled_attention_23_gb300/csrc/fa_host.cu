@@ -11,7 +11,9 @@
 // that the other's longest work items (the last query tiles under a causal
 // mask) leave idle.  The caller provides the device buffers, so the library
 // still allocates no device memory; it keeps four streams and a ring of
-// events per device.
+// events per device.  Calls on one device from several host threads take
+// turns: each enqueues its whole sequence under that device's lock, so no
+// call's event records fall between another's records and waits.
 #include "fa.h"
 #include "fa_internal.h"
 
@@ -32,9 +34,11 @@ struct CopyStreams {
     cudaStream_t comp[2] = {};
     cudaEvent_t start = nullptr;
     cudaEvent_t done = nullptr;
+    cudaEvent_t comp_end[2] = {};
     cudaEvent_t in_ready[kEventRing] = {};
     cudaEvent_t out_ready[kEventRing] = {};
     bool ready = false;
+    std::mutex enqueue;   // held by a call from its first record to its last wait
 };
 
 std::mutex g_mu;
@@ -55,7 +59,9 @@ fa_status copy_streams(CopyStreams **out)
                   cudaStreamCreateWithFlags(&cs.comp[0], cudaStreamNonBlocking) == cudaSuccess &&
                   cudaStreamCreateWithFlags(&cs.comp[1], cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&cs.start, flags) == cudaSuccess &&
-                  cudaEventCreateWithFlags(&cs.done, flags) == cudaSuccess;
+                  cudaEventCreateWithFlags(&cs.done, flags) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&cs.comp_end[0], flags) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&cs.comp_end[1], flags) == cudaSuccess;
         for (int i = 0; ok && i < kEventRing; ++i)
             ok = cudaEventCreateWithFlags(&cs.in_ready[i], flags) == cudaSuccess &&
                  cudaEventCreateWithFlags(&cs.out_ready[i], flags) == cudaSuccess;
@@ -148,47 +154,62 @@ extern "C" fa_status fa_fwd_from_host(const void *Q_host, const void *K_host, co
     // that the result is fa_fwd's exactly (the kernels agree only to rounding).
     const int tiles = fa::fwd16_tiles(B, H, N, D);
 
-    // Earlier work on the caller's stream may still use the buffers.
-    FA_TRY(cudaEventRecord(cs->start, user));
-    FA_TRY(cudaStreamWaitEvent(cs->h2d, cs->start, 0));
-    FA_TRY(cudaStreamWaitEvent(cs->d2h, cs->start, 0));
-    FA_TRY(cudaStreamWaitEvent(cs->comp[0], cs->start, 0));
-    FA_TRY(cudaStreamWaitEvent(cs->comp[1], cs->start, 0));
+    std::lock_guard<std::mutex> turn(cs->enqueue);
     // Events are reused round-robin.  That is safe because each record is
     // followed, in host order, by the wait that consumes it: a wait takes
     // the work of the most recent record at the time it is enqueued.
-    int c = 0;
-    for (int b = 0; b < B; ++b) {
-        for (int h0 = 0; h0 < H; h0 += hc_max, ++c) {
-            const int hc = (H - h0) < hc_max ? (H - h0) : hc_max;
-            const size_t first = (size_t)b * H + (size_t)h0;        // first (b, h) slice of the group
-            const size_t off = first * head_elems * es, bytes = (size_t)hc * head_elems * es;
-            const size_t loff = first * (size_t)N * sizeof(float), lbytes = (size_t)hc * N * sizeof(float);
-            cudaEvent_t in = cs->in_ready[c % kEventRing], outv = cs->out_ready[c % kEventRing];
-            FA_TRY(h2d(Q_dev, Q_host, off, bytes));
-            FA_TRY(h2d(K_dev, K_host, off, bytes));
-            FA_TRY(h2d(V_dev, V_host, off, bytes));
-            FA_TRY(cudaEventRecord(in, cs->h2d));
-            cudaStream_t comp = cs->comp[c & 1];
-            FA_TRY(cudaStreamWaitEvent(comp, in, 0));
-            char *qd = static_cast<char *>(Q_dev) + off;
-            char *kd = static_cast<char *>(K_dev) + off;
-            char *vd = static_cast<char *>(V_dev) + off;
-            char *od = static_cast<char *>(O_dev) + off;
-            float *ld = LSE_dev ? LSE_dev + first * (size_t)N : nullptr;
-            const int32_t *kl = kv_len ? kv_len + b : nullptr;
-            st = fa::fwd16_with_tiles(qd, kd, vd, od, ld, 1, hc, N, D, causal, scale, kl, f16 != 0, tiles, comp);
-            if (st != FA_OK) return st;
-            FA_TRY(cudaEventRecord(outv, comp));
-            FA_TRY(cudaStreamWaitEvent(cs->d2h, outv, 0));
-            FA_TRY(d2h(O_host, O_dev, off, bytes));
-            if (LSE_host) FA_TRY(d2h(LSE_host, LSE_dev, loff, lbytes));
+    auto enqueue_groups = [&]() -> fa_status {
+        // Earlier work on the caller's stream may still use the buffers.
+        FA_TRY(cudaEventRecord(cs->start, user));
+        FA_TRY(cudaStreamWaitEvent(cs->h2d, cs->start, 0));
+        FA_TRY(cudaStreamWaitEvent(cs->d2h, cs->start, 0));
+        FA_TRY(cudaStreamWaitEvent(cs->comp[0], cs->start, 0));
+        FA_TRY(cudaStreamWaitEvent(cs->comp[1], cs->start, 0));
+        int c = 0;
+        for (int b = 0; b < B; ++b) {
+            for (int h0 = 0; h0 < H; h0 += hc_max, ++c) {
+                const int hc = (H - h0) < hc_max ? (H - h0) : hc_max;
+                const size_t first = (size_t)b * H + (size_t)h0;        // first (b, h) slice of the group
+                const size_t off = first * head_elems * es, bytes = (size_t)hc * head_elems * es;
+                const size_t loff = first * (size_t)N * sizeof(float), lbytes = (size_t)hc * N * sizeof(float);
+                cudaEvent_t in = cs->in_ready[c % kEventRing], outv = cs->out_ready[c % kEventRing];
+                FA_TRY(h2d(Q_dev, Q_host, off, bytes));
+                FA_TRY(h2d(K_dev, K_host, off, bytes));
+                FA_TRY(h2d(V_dev, V_host, off, bytes));
+                FA_TRY(cudaEventRecord(in, cs->h2d));
+                cudaStream_t comp = cs->comp[c & 1];
+                FA_TRY(cudaStreamWaitEvent(comp, in, 0));
+                char *qd = static_cast<char *>(Q_dev) + off;
+                char *kd = static_cast<char *>(K_dev) + off;
+                char *vd = static_cast<char *>(V_dev) + off;
+                char *od = static_cast<char *>(O_dev) + off;
+                float *ld = LSE_dev ? LSE_dev + first * (size_t)N : nullptr;
+                const int32_t *kl = kv_len ? kv_len + b : nullptr;
+                const fa_status gs =
+                    fa::fwd16_with_tiles(qd, kd, vd, od, ld, 1, hc, N, D, causal, scale, kl, f16 != 0, tiles, comp);
+                if (gs != FA_OK) return gs;
+                FA_TRY(cudaEventRecord(outv, comp));
+                FA_TRY(cudaStreamWaitEvent(cs->d2h, outv, 0));
+                FA_TRY(d2h(O_host, O_dev, off, bytes));
+                if (LSE_host) FA_TRY(d2h(LSE_host, LSE_dev, loff, lbytes));
+            }
         }
-    }
-    // The caller's stream completes only when every output is in host memory
-    // (the copy-out stream has waited for every group's computation).
-    FA_TRY(cudaEventRecord(cs->done, cs->d2h));
-    FA_TRY(cudaStreamWaitEvent(user, cs->done, 0));
+        return FA_OK;
+    };
+    st = enqueue_groups();
+    // Whether or not every group was enqueued, the caller's stream goes on
+    // only after everything this call put on the library's streams: the
+    // copy-out stream waits for the end of both compute streams (on success
+    // it has already waited for every group's computation), and the caller's
+    // stream waits for the copy-out stream.  So a caller that frees or reuses
+    // the buffers after an error does not race with work still in flight.
+    const bool fenced = cudaEventRecord(cs->comp_end[0], cs->comp[0]) == cudaSuccess &&
+                        cudaEventRecord(cs->comp_end[1], cs->comp[1]) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs->d2h, cs->comp_end[0], 0) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs->d2h, cs->comp_end[1], 0) == cudaSuccess &&
+                        cudaEventRecord(cs->done, cs->d2h) == cudaSuccess &&
+                        cudaStreamWaitEvent(user, cs->done, 0) == cudaSuccess;
+    if (st != FA_OK) return st;
 #undef FA_TRY
-    return FA_OK;
+    return fenced ? FA_OK : FA_ERR_CUDA;
 }

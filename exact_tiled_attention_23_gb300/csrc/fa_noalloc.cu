@@ -21,8 +21,9 @@
 #include <cstddef>
 #include <mutex>
 
-// The scratch every call shares.  Every GPU that loads this library holds it
-// until the process exits.
+// The scratch every call shares.  A device holds it from the time this
+// library's code is loaded there (under lazy module loading, the first call of
+// the entry point at the latest) until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -31,7 +32,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch on the current device (looked up once per device).
+// Device address of the scratch on the current device, looked up once per
+// device and kept for the life of the process (a cudaDeviceReset, which may
+// move the array, is not followed: the header says so).
 fa_status scratch_on_current_device(void **out)
 {
     int dev = 0;

@@ -4,6 +4,8 @@
 // instruction (or a short fixed sequence) written from the PTX ISA.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include <cstdint>
 
 namespace fa {
@@ -170,6 +172,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "r"(taddr));
 }
 
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(
@@ -229,6 +243,7 @@ __device__ __forceinline__ uint32_t pack16x2(float lo, float hi)
         return pack_bf16x2(lo, hi);
 }
 
+
 }  // namespace ptx
 }  // namespace fa
 
@@ -268,6 +283,20 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// The two 16-bit values of `w` (f16 when kF16, else bf16; low half first)
+// as a packed fp32 pair, exactly.
+template <bool kF16>
+__device__ __forceinline__ uint64_t widen16x2(uint32_t w)
+{
+    if constexpr (kF16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+        return pack2(f.x, f.y);
+    } else {
+        // a bf16 value is the upper half of the fp32 with the same value
+        return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
 }
 
 // max of three fp32 values in one instruction

@@ -162,9 +162,10 @@ int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D);
  * and output buffers, or a real-time loop where an allocation could block.
  * This entry point takes no workspace.  It uses a fixed scratch array of
  * FA_NOALLOC_SCRATCH_BYTES bytes that the library keeps in device memory.
- * Every GPU that loads the library holds that array until the process exits.
- * The call itself allocates nothing: no cudaMalloc, no cudaFree, no
- * allocating library routine.
+ * A device holds that array from the time the library's code is loaded on
+ * it (with CUDA's lazy module loading, the first call of this entry point
+ * there at the latest) until the process exits.  The call itself allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *
  * Arguments are those of fa_fwd_splitkv without the workspace.  The caller
  * still passes the inputs and outputs.
@@ -175,8 +176,11 @@ int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D);
  *     before anything is enqueued.  Fewer splits, or fa_fwd, are the
  *     alternatives.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current.  Make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and later calls on
+ *     that device reuse it.  Make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset of a device this entry point must not be called on it
+ *     again, because the array may then sit at another address.
  *   - All calls share the one array, and it keeps the last call's contents.
  *     Each call rewrites every part it reads, so nothing needs clearing.
  *   - Two calls whose kernels overlap on the GPU (different streams, or
@@ -223,8 +227,12 @@ fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, vo
  *
  * Returns as fa_fwd; all argument checks run before any CUDA call.  The first
  * call on a device creates that device's four streams and their events.
- * Calls on one device share them, so calls from different host threads are
- * serialised on the copy engines.
+ * Calls on one device share them.  Calls from several host threads are safe:
+ * each enqueues its whole sequence of copies, launches and event records
+ * under a per-device lock, so the calls run one after another on the
+ * library's streams.  If a CUDA call fails partway, the caller's stream
+ * still waits for everything the call had enqueued before the failure, so
+ * the buffers may be freed or reused once that stream reaches this point.
  */
 #define FA_MAX_HOST_GROUPS 1024
 

@@ -6,9 +6,10 @@ sees at least one key; LSE within 1e-3 + 1e-5*|LSE|.  fp32 path:
 max |O - O_ref| <= 1e-5 and |LSE - LSE_ref| <= 1e-5 * max(1, |LSE|).
 Rows that see no key must be exact +0.0 with LSE = -inf (bitwise checks).
 
-Small cases compare every element; the full-size workloads are run in the
-launch configuration the benchmark times and compared on sampled rows that
-the oracle computes one by one, plus properties checked on every row.
+Small cases and the full-size workloads (run in the launch configuration
+the benchmark times) are compared on every element; the non-default kernel
+at full size and a few other full-size runs on sampled rows that the oracle
+computes one by one.
 """
 import math
 
@@ -140,6 +141,23 @@ def test_bf16_large_logits(D, tiles):
     q[:, :, ::5] *= 30.0
     q[:, :, 1::7] *= -30.0
     inp.q = q.to(torch.bfloat16)
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_bf16_dominant_weight_rows(D, causal, tiles):
+    """Every query row x30, V up to 5.9 in magnitude: the rows are close to
+    one-hot, and the key holding most of the weight usually lies past the
+    block that set the row's reference max, so its p is not 1 and its bf16
+    rounding is up to 2^-8 relative.  O must be normalised by the sum of the
+    rounded P the MMA multiplies V by; normalised by the fp32 sum of p, a CPU
+    model of the kernel's rounding puts max |dO| at 0.024-0.032 here, above
+    the 2e-2 bound."""
+    inp = workloads.make_case(1, 2, 1024, D, dtype="bf16", causal=causal, seed=23 + D)
+    inp.q = (inp.q.float() * 30.0).to(torch.bfloat16)
+    inp.v = (inp.v.float() * 1.5).clamp(-5.9, 5.9).to(torch.bfloat16)
     o, lse = run_gpu(inp)
     compare(inp, o, lse)
 
@@ -389,6 +407,44 @@ def test_from_host_without_lse_and_on_a_side_stream():
     assert torch.equal(oh, o_ref.cpu())
 
 
+def test_from_host_from_two_threads():
+    """Two host threads call fa_fwd_from_host at once on the same device, on
+    separate buffers and streams, several times each.  The calls share the
+    library's copy streams and events, and take turns enqueueing; every
+    result equals fa_fwd's."""
+    import threading
+
+    cases = []
+    for t, (causal, kv) in enumerate([(True, [300, 0, 123]), (False, [17, 300, 299])]):
+        inp = workloads.make_case(3, 4, 300, 64, dtype="bf16", causal=causal, seed=50 + t, kv_len=kv)
+        kvd = inp.kv_len.cuda()
+        o_ref, l_ref = fa.forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), causal=causal, kv_len=kvd)
+        cases.append((inp, kvd, o_ref.cpu(), l_ref.cpu()))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(t):
+        try:
+            inp, kvd, o_ref, l_ref = cases[t]
+            qh, kh, vh = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+            s = torch.cuda.Stream()
+            for rep in range(6):
+                o, lse = fa.forward_from_host(qh, kh, vh, causal=inp.causal, kv_len=kvd, groups=3 + rep % 2,
+                                              stream=s)
+                if not (torch.equal(o, o_ref) and torch.equal(lse, l_ref)):
+                    errors.append(f"thread {t} call {rep}: result differs from fa_fwd")
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(f"thread {t}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert fa.fa_device_status(None) == fa.FA_OK
+
+
 def test_outputs_are_deterministic(tiles):
     inp = workloads.make_case(2, 4, 777, 128, dtype="bf16", causal=True, seed=3, kv_len=[777, 400])
     o1, l1 = run_gpu(inp)
@@ -440,24 +496,87 @@ def sample_rows(inp, n_random=768, seed=0):
     return np.array(sorted(rows), dtype=np.int64)
 
 
+def compare_every_row(inp, o_gpu, lse_gpu):
+    """Every row of every head against the oracle, one batch at a time.
+
+    Returns per-head error figures [B, H, 3]: max |dO|, mean |dO| over the
+    head's live rows, max |dLSE|.  The tolerances of `compare` hold for each
+    head on its own and for the whole workload.
+    """
+    w = inp.workload
+    B, H, N, D = w.B, w.H, w.N, w.D
+    qf, kf, vf = (x.float().numpy() for x in (inp.q, inp.k, inp.v))
+    kv = None if inp.kv_len is None else inp.kv_len.numpy()
+    stats = np.zeros((B, H, 3))
+    err_sum, n_live = 0.0, 0
+    for b in range(B):
+        kvb = None if kv is None else kv[b:b + 1]
+        o_ref, lse_ref = oracle.attention(qf[b:b + 1], kf[b:b + 1], vf[b:b + 1], causal=inp.causal,
+                                          scale=w.scale, kv_len=kvb)
+        o_ref, lse_ref = o_ref[0], lse_ref[0]
+        og = o_gpu[b].float().cpu().numpy().astype(np.float64)
+        lg = lse_gpu[b].cpu().numpy().astype(np.float64)
+        L = N if kv is None else int(np.clip(kv[b], 0, N))
+        i = np.arange(N)
+        live = (np.minimum(L, i + 1) if inp.causal else np.full(N, L)) > 0
+        assert np.all(np.isfinite(og)), f"batch {b}: non-finite O"
+        if np.any(~live):
+            dead = og[:, ~live]
+            assert np.all(dead == 0.0) and not np.any(np.signbit(dead)), f"batch {b}: masked rows not exact +0"
+            assert np.all(np.isneginf(lg[:, ~live])), f"batch {b}: masked rows' LSE not -inf"
+        if not np.any(live):
+            continue
+        assert np.all(np.isfinite(lg[:, live])), f"batch {b}: non-finite LSE on a live row"
+        err = np.abs(og[:, live] - o_ref[:, live])               # [H, live, D]
+        lerr = np.abs(lg[:, live] - lse_ref[:, live])            # [H, live]
+        stats[b, :, 0] = err.max(axis=(1, 2))
+        stats[b, :, 1] = err.mean(axis=(1, 2))
+        stats[b, :, 2] = lerr.max(axis=1)
+        err_sum += float(err.sum())
+        n_live += err.size
+        if w.dtype == "fp32":
+            lbound = 1e-5 * np.maximum(1.0, np.abs(lse_ref[:, live]))
+        else:
+            lbound = 1e-3 + 1e-5 * np.abs(lse_ref[:, live])
+        assert np.all(lerr <= lbound), f"batch {b}: LSE err {lerr.max()}"
+    table = "\n".join(f"  b={b} h={h}: max {stats[b, h, 0]:.3e} mean {stats[b, h, 1]:.3e} "
+                      f"lse {stats[b, h, 2]:.3e}" for b in range(B) for h in range(H))
+    if w.dtype == "fp32":
+        assert stats[..., 0].max() <= FP32_MAX, "fp32 max err per head:\n" + table
+    else:
+        assert stats[..., 0].max() <= BF16_MAX, "bf16 max err per head:\n" + table
+        assert stats[..., 1].max() <= BF16_MEAN, "bf16 mean err per head:\n" + table
+        assert err_sum / max(n_live, 1) <= BF16_MEAN
+    return stats
+
+
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
 def test_full_workload(name):
+    """Each workload at its full size, in the launch configuration the
+    benchmark times, compared with the oracle on every element."""
     inp = workloads.make(name)
     o, lse = run_gpu(inp)
     w = inp.workload
-    # properties on every row
-    assert not torch.isnan(o).any() and not torch.isinf(o).any()
     assert not torch.isnan(lse).any()
-    if inp.kv_len is not None:
-        for b in range(w.B):
-            if int(inp.kv_len[b]) == 0:
-                assert bool((o[b] == 0).all()) and not bool(torch.signbit(o[b].float()).any())
-                assert bool(torch.isneginf(lse[b]).all())
     assert not torch.isneginf(lse).any() or inp.kv_len is not None
-    if w.B * w.H * w.N <= 4096:
-        compare(inp, o, lse)
-    else:
-        compare(inp, o, lse, rows=sample_rows(inp, seed=w.index))
+    stats = compare_every_row(inp, o, lse)
+    print(f"{name}: per-head max |dO| <= {stats[..., 0].max():.3e}, "
+          f"per-head mean |dO| <= {stats[..., 1].max():.3e}, max |dLSE| {stats[..., 2].max():.3e}")
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].dtype != "fp32"])
+def test_full_workload_other_kernel(name, monkeypatch):
+    """The tensor-core kernel the library does not choose for this workload
+    (one or two query tiles per CTA), forced, at full size: sampled rows
+    against the oracle."""
+    inp = workloads.make(name)
+    w = inp.workload
+    items = w.B * w.H * -(-w.N // 256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chosen = "1" if 2 * items <= sms else "2"
+    monkeypatch.setenv("FA_FWD_TILES", "2" if chosen == "1" else "1")
+    o, lse = run_gpu(inp)
+    compare(inp, o, lse, rows=sample_rows(inp, seed=w.index))
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
