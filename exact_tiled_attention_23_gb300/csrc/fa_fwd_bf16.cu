@@ -59,6 +59,12 @@ constexpr int BM = 128;          // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;          // keys per step
 constexpr int kThreads = 384;    // 12 warps
 constexpr int kFirstSoftmaxWarp = 4;
+// setmaxnreg split: the control warpgroup's and the softmax warpgroups'
+// registers per thread, which must fit the block's launch allocation (384
+// threads x 168) or setmaxnreg.inc would wait forever.
+constexpr int kRegsControl = 96;
+constexpr int kRegsSoftmax = 200;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * ((65536 / kThreads) / 8 * 8), "register split");
 
 template <int D>
 struct Layout {
@@ -168,7 +174,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // the 384*168 registers the CTA is launched with.  Each setmaxnreg sits
     // in the branch of the role it serves.
     if (warp < kFirstSoftmaxWarp) {
-    ptx::regs_dec<96>();
+    ptx::regs_dec<kRegsControl>();
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && n_kv > 0) {
@@ -287,7 +293,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     }
     } else {
-        ptx::regs_inc<200>();
+        ptx::regs_inc<kRegsSoftmax>();
         // ================= online softmax + epilogue =================
         const int i = (warp - kFirstSoftmaxWarp) / 4;      // query tile of this warpgroup
         const int quarter = warp & 3;                      // TMEM lanes 32*quarter ..

@@ -69,7 +69,7 @@ def test_a_wait_that_runs_out_reports_a_timeout(case, tiles):
     if tiles:
         env["FA_FWD_TILES"] = tiles
     run = subprocess.run([sys.executable, "-c", CHILD, case, ROOT], env=env, capture_output=True,
-                         text=True, timeout=600)
+                         text=True, timeout=120)
     assert run.returncode == 0, run.stderr[-2000:]
     result = json.loads(run.stdout.strip().splitlines()[-1])
     assert result["status"] == FA_ERR_TIMEOUT, result
