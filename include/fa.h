@@ -17,9 +17,14 @@
  * Layout (all arguments): Q, K, V and O are contiguous row-major
  * [B, H, N, D] arrays; LSE is a contiguous [B, H, N] float array; kv_len is
  * an int32 array of B entries.  Every pointer is DEVICE memory owned by the
- * caller; the library allocates no device memory, keeps no pointer after the
- * call returns, and its only state is a device-side status word (see
- * fa_device_status) and a cached driver entry point.
+ * caller unless stated otherwise (fa_fwd_from_host takes host arrays); no
+ * call allocates device memory or keeps a pointer after it returns.  The
+ * library's own state is: device-side status words (see fa_device_status); a
+ * cached driver entry point; the fixed scratch array of
+ * fa_fwd_splitkv_noalloc (FA_NOALLOC_SCRATCH_BYTES of device memory, held from
+ * the time the library's code is loaded on a device); and, per device that
+ * calls fa_fwd_from_host, four streams and a set of events, created by the
+ * first such call and kept for the life of the process.
  *
  * Calls are asynchronous: they validate their arguments on the host, enqueue
  * one kernel on `stream` (a cudaStream_t; NULL = the legacy default stream)
@@ -32,7 +37,12 @@
  *     exactness", Root causes 2);
  *   - query rows at or past kv_len[b] are still computed over the keys
  *     j < kv_len[b] (padding hides keys, not queries);
- *   - kv_len entries outside [0, N] are clamped to that range on the device.
+ *   - kv_len entries outside [0, N] are clamped to that range on the device;
+ *   - input range: the 16-bit paths keep each key block's weights p against a
+ *     reference that moves only when a block's sum of p would pass 2^64
+ *     (bf16) or 2^15 (fp16), so the fp32 output accumulator holds up to
+ *     N * 2^64 * max|V|; O is finite for bf16 |V| < 2^32 (any N < 2^31) and
+ *     for every fp16 V.  Q and K may take any finite values.
  */
 #ifndef EXACT_TILED_ATTENTION_FA_H
 #define EXACT_TILED_ATTENTION_FA_H
@@ -85,7 +95,9 @@ typedef enum fa_status {
  * one of them (D = 256 always runs the one-tile kernel).
  *
  * Accumulation is fp32 (scores, running sums, O); P is rounded to bf16 for
- * the second product.  Returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED from
+ * the second product, and O is divided by the sum of those rounded weights
+ * (the LSE uses the sum of the unrounded ones), so O is a convex combination
+ * of V rows whatever the rounding.  Returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED from
  * host-side checks before anything is enqueued, FA_ERR_CUDA if the launch
  * fails.
  */
