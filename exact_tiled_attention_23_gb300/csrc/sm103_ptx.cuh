@@ -244,11 +244,6 @@ __device__ __forceinline__ uint32_t pack16x2(float lo, float hi)
 }
 
 
-}  // namespace ptx
-}  // namespace fa
-
-namespace fa {
-namespace ptx {
 
 // ---------------------------------------------------------------- packed fp32
 // Blackwell executes two fp32 lanes per instruction with the .f32x2 forms.
@@ -321,11 +316,6 @@ __device__ __forceinline__ void regs_inc()
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-}  // namespace ptx
-}  // namespace fa
-
-namespace fa {
-namespace ptx {
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads, TMA).
@@ -348,11 +338,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
                  : "memory");
 }
 
-}  // namespace ptx
-}  // namespace fa
-
-namespace fa {
-namespace ptx {
 
 // Named barrier `id` (1..15) over `nthreads` threads of the CTA (a multiple of 32).
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t nthreads)
@@ -360,11 +345,6 @@ __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-}  // namespace ptx
-}  // namespace fa
-
-namespace fa {
-namespace ptx {
 
 // Named barrier `id` over `nthreads` threads that also returns the AND of
 // `pred` over them (every participant gets the same answer).
@@ -382,11 +362,6 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool pre
     return r != 0;
 }
 
-}  // namespace ptx
-}  // namespace fa
-
-namespace fa {
-namespace ptx {
 
 // 3-D tiled reduce-add of one shared-memory box into global memory (fp32
 // adds done by the TMA engine); completion is tracked with bulk groups.
@@ -422,11 +397,6 @@ __device__ __forceinline__ void bulk_wait_group_read()
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-}  // namespace ptx
-}  // namespace fa
-
-namespace fa {
-namespace ptx {
 
 // Wait until every committed bulk group of this thread has completed (its
 // global writes included).
