@@ -159,15 +159,34 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ptx::mbar_init(mma_drain, 1);
         *abort_word = 0;
         ptx::fence_mbarrier_init();
+        // Thread 0 is also the producer: the item's Q tiles and K_0 (pair 0)
+        // are requested now, so that their latency overlaps the TMEM
+        // allocation and the CTA-wide barrier below.
+        if (n_kv > 0) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::mbar_arrive_expect_tx(q_full, 2 * Lay::kTileBytes);
+            for (int i = 0; i < 2; ++i)
+                for (int c = 0; c < Lay::kChunks; ++c)
+                    ptx::tma_load_3d(smem + Lay::kQOff + i * Lay::kTileBytes + c * Lay::kChunkBytes,
+                                     &tm_q, q_full, c * 64, (int32_t)(q0 + i * BM), (int32_t)bh);
+            ptx::mbar_arrive_expect_tx(&pair_full[0], Lay::kTileBytes);
+            for (int c = 0; c < Lay::kChunks; ++c)
+                ptx::tma_load_3d(smem + Lay::kKVOff + c * Lay::kChunkBytes, &tm_k, &pair_full[0], c * 64,
+                                 (int32_t)(blk0 * BN), (int32_t)bh);
+        }
     }
-    if (warp == 1) {
+    // An item with no visible key only writes O = 0 and LSE = -inf: it needs
+    // no tensor memory.
+    if (warp == 1 && n_kv > 0) {
         ptx::tmem_alloc(tmem_slot, Lay::kTmemCols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = n_kv > 0 ? *tmem_slot : 0u;
 
     // Registers: the producer / MMA warpgroup needs few; the softmax
     // warpgroups hold a 128-column score row each.  128*96 + 256*200 fits in
@@ -178,19 +197,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && n_kv > 0) {
-            ptx::tma_prefetch_desc(&tm_q);
-            ptx::tma_prefetch_desc(&tm_k);
-            ptx::tma_prefetch_desc(&tm_v);
-            ptx::mbar_arrive_expect_tx(q_full, 2 * Lay::kTileBytes);
-            for (int i = 0; i < 2; ++i)
-                for (int c = 0; c < Lay::kChunks; ++c)
-                    ptx::tma_load_3d(smem + Lay::kQOff + i * Lay::kTileBytes + c * Lay::kChunkBytes,
-                                     &tm_q, q_full, c * 64, (int32_t)(q0 + i * BM), (int32_t)bh);
-            // Pair m (0 <= m <= n_kv) holds V_{m-1} in slot 2m-1 and K_m in
-            // slot 2m (mod kSlots); from m = kPairs on, those slots are the
-            // ones of pair m - kPairs, which the MMA warp must have released.
-            int pairs_armed = 0;    // pairs 0 .. pairs_armed-1 have had their copies issued
-            for (int m = 0; m <= n_kv; ++m) {
+            // Q and pair 0 (K_0 alone) were requested before the CTA-wide
+            // barrier.  Pair m (0 <= m <= n_kv) holds V_{m-1} in slot 2m-1 and
+            // K_m in slot 2m (mod kSlots); from m = kPairs on, those slots are
+            // the ones of pair m - kPairs, which the MMA warp must have released.
+            int pairs_armed = 1;    // pairs 0 .. pairs_armed-1 have had their copies issued
+            for (int m = 1; m <= n_kv; ++m) {
                 if (m >= Lay::kPairs) {
                     const int pm = m - Lay::kPairs;
                     if (!wait_bounded(&pair_empty[pm % Lay::kPairs], (pm / Lay::kPairs) & 1, p.wait_limit_ns,
@@ -431,7 +443,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- teardown ----------------------------------------------------------
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 1 && n_kv > 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, Lay::kTmemCols);
     }

@@ -131,32 +131,44 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             ptx::mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? 4 : 1);
         *abort_word = 0;
         ptx::fence_mbarrier_init();
+        // Thread 0 is also the producer: Q and K_0 are requested now, so that
+        // their latency overlaps the TMEM allocation and the barrier below.
+        if (n_kv > 0) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::mbar_arrive_expect_tx(q_full, kTileBytes);
+            for (int c = 0; c < kChunks; ++c)
+                ptx::tma_load_3d(smem + kQOff + c * kChunkBytes, &tm_q, q_full, c * 64, (int32_t)q0, (int32_t)bh);
+            ptx::mbar_arrive_expect_tx(&k_full[0], kTileBytes);
+            for (int c = 0; c < kChunks; ++c)
+                ptx::tma_load_3d(smem + kKOff + c * kChunkBytes, &tm_k, &k_full[0], c * 64, 0, (int32_t)bh);
+        }
     }
-    if (warp == 1) {
+    // An item with no visible key only writes O = 0 and LSE = -inf: it needs
+    // no tensor memory.
+    if (warp == 1 && n_kv > 0) {
         ptx::tmem_alloc(tmem_slot, kTmemCols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = n_kv > 0 ? *tmem_slot : 0u;
 
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && n_kv > 0) {
-            ptx::tma_prefetch_desc(&tm_q);
-            ptx::tma_prefetch_desc(&tm_k);
-            ptx::tma_prefetch_desc(&tm_v);
             auto load_tile = [&](const CUtensorMap *tm, int off, uint64_t *bar, int64_t row0) {
                 ptx::mbar_arrive_expect_tx(bar, kTileBytes);
                 for (int c = 0; c < kChunks; ++c)
                     ptx::tma_load_3d(smem + off + c * kChunkBytes, tm, bar, c * 64, (int32_t)row0, (int32_t)bh);
             };
-            load_tile(&tm_q, kQOff, q_full, q0);
             // Loads in the order the MMAs read them: K_0, K_1, then V_t and
-            // K_{t+2} in turn.  K_t goes into slot t % R once S_{t-R} has read
-            // that slot, V_t once O += P_{t-R} V_{t-R} has.
-            int k_issued = 0, v_issued = 0;
+            // K_{t+2} in turn (Q and K_0 were requested before the CTA-wide
+            // barrier).  K_t goes into slot t % R once S_{t-R} has read that
+            // slot, V_t once O += P_{t-R} V_{t-R} has.
+            int k_issued = 1, v_issued = 0;
             auto load_k = [&]() -> bool {
                 const int t = k_issued;
                 if (t >= R &&
@@ -175,8 +187,8 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 ++v_issued;
                 return true;
             };
-            bool ok = load_k();
-            if (ok && n_kv > 1) ok = load_k();
+            bool ok = true;
+            if (n_kv > 1) ok = load_k();
             while (ok && v_issued < n_kv) {
                 ok = load_v();
                 if (ok && k_issued < n_kv) ok = load_k();
@@ -364,7 +376,7 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // ---- teardown ----------------------------------------------------------
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 1 && n_kv > 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
