@@ -13,12 +13,19 @@
 //     dimension below 64 / 128 reads zero-filled columns).  The tiles move in
 //     the pairs the MMA warp consumes together, (V_j, K_{j+1}): one barrier
 //     signals a pair's arrival and one commit its release;
-//   * warp 1 issues every tcgen05.mma: S_i = Q_i K_j^T (both operands in
-//     shared memory) and O_i += P_i V_j (P_i read from tensor memory);
+//   * warp 1 issues the tcgen05.mma products: S_i = Q_i K_j^T (both
+//     operands in shared memory) and O_i += P_i V_j (P_i read from tensor
+//     memory).  At D = 64, where P_i has TMEM columns of its own, warp 3
+//     issues the S products instead, as soon as the softmax warps hold the
+//     previous S_i in registers, so S_i(j+1) is computed while they work on
+//     block j and the two products of a tile come from two threads (one
+//     thread issues at most one N=128 product per ~90-100 clk on this GPU;
+//     two keep the tensor core at its 64 clk rate);
 //   * warps 4-7 and 8-11 run the online softmax of tile 0 and tile 1: each
 //     thread loads its row of S_i from TMEM, masks, updates the running max m
-//     and sum l, writes P_i = exp2(S*scale*log2e - m) as bf16 back into the
-//     same TMEM columns, and rescales O_i in TMEM when the max moved;
+//     and sum l, writes P_i = exp2(S*scale*log2e - m) as bf16 back into TMEM
+//     (over S_i at D = 128, into P_i's own columns at D = 64), and rescales
+//     O_i in TMEM when the max moved;
 //   * while one tile's softmax runs, the tensor core works on the other tile,
 //     so the two softmax warpgroups alternate with the MMAs;
 //   * at the end each tile's warps stage O (16-bit) in the tile's Q buffer and
@@ -64,6 +71,9 @@ constexpr int kFirstSoftmaxWarp = 4;
 // threads x 168) or setmaxnreg.inc would wait forever.
 constexpr int kRegsControl = 96;
 constexpr int kRegsSoftmax = 200;
+// P apart (D = 64): chunks of 32 scores a softmax thread exponentiates before
+// it waits for the previous PV product and stores P.
+constexpr int kEarlyChunks = 2;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * ((65536 / kThreads) / 8 * 8), "register split");
 
 template <int D>
@@ -84,12 +94,18 @@ struct Layout {
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;   // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
     // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 after it.
-    // P_i (bf16 pairs) overwrites the first 64 columns of S_i.
+    // At D = 128 P_i (16-bit pairs) overwrites the first 64 columns of S_i.
+    // At D = 64 the O tiles leave 128 columns free and P_i has 64 of its own
+    // (kPApart): O_i += P_i V_j and S_i = Q_i K_{j+1}^T then touch disjoint
+    // columns, and two threads issue them side by side (see the MMA roles).
+    static constexpr bool kPApart = (D == 64);
     __device__ static constexpr uint32_t col_s(int i) { return (uint32_t)i * 128u; }
     __device__ static constexpr uint32_t col_o(int i) { return 256u + (uint32_t)i * D; }
+    __device__ static constexpr uint32_t col_p(int i) { return kPApart ? 384u + (uint32_t)i * 64u : col_s(i); }
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(!kPApart || 256 + 2 * D + 2 * 64 <= (int)kTmemCols, "P tiles of their own");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert((1 + 2 * kPairs + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((1 + 2 * kPairs + 12) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 
@@ -115,7 +131,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t *p_full = s_full + 2;                 // [2]
     uint64_t *o_final = p_full + 2;                // [2]
     uint64_t *mma_drain = o_final + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
+    // P apart (D = 64) only: PV_i of a block done (its P columns may be
+    // rewritten, O_i rescaled); S_i of a block loaded into the softmax
+    // warps' registers (its columns may be rewritten); the drain of the
+    // second MMA thread.
+    uint64_t *pv_done = mma_drain + 1;             // [2]
+    uint64_t *s_read = pv_done + 2;                // [2]
+    uint64_t *mma_drain_s = s_read + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain_s + 1);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     const Abort ab{abort_word, &g_status};
 
@@ -149,14 +172,18 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ptx::mbar_init(q_full, 1);
         for (int s = 0; s < Lay::kPairs; ++s) {
             ptx::mbar_init(&pair_full[s], 1);
-            ptx::mbar_init(&pair_empty[s], 1);
+            // with two MMA threads, each releases every pair once
+            ptx::mbar_init(&pair_empty[s], Lay::kPApart ? 2 : 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s_full[i], 1);
             ptx::mbar_init(&p_full[i], 4);          // one arrival per softmax warp
             ptx::mbar_init(&o_final[i], 1);
+            ptx::mbar_init(&pv_done[i], 1);
+            ptx::mbar_init(&s_read[i], 4);          // one arrival per softmax warp
         }
         ptx::mbar_init(mma_drain, 1);
+        ptx::mbar_init(mma_drain_s, 1);
         *abort_word = 0;
         ptx::fence_mbarrier_init();
         // Thread 0 is also the producer: the item's Q tiles and K_0 (pair 0)
@@ -228,8 +255,15 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 wait_bounded(&pair_full[m % Lay::kPairs], (m / Lay::kPairs) & 1, p.wait_limit_ns, kSiteDrain,
                              ab, false);
         }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
+    } else if (warp == 1 || (Lay::kPApart && warp == 3)) {
+        // ================= MMA issuers =================
+        // D = 128: warp 1 issues every product, PV_0(j), S_0(j+1), PV_1(j),
+        // S_1(j+1) in turn, which keeps S_i(j+1) behind the PV_i(j) that
+        // reads the P columns it overwrites.  D = 64 (P apart): warp 1 issues
+        // the PV products and warp 3 the S products.  The two streams share no
+        // TMEM columns, and two issuing threads keep the tensor core busier
+        // than one: a probe on this GPU ran one thread's N=128 products at
+        // ~110 clk each and two threads' at ~70 clk per product together.
         if (lane == 0 && n_kv > 0) {
             constexpr uint32_t idesc_qk = make_idesc(BM, BN, 0, 0, kF16);
             constexpr uint32_t idesc_pv = make_idesc(BM, D, 0, 1, kF16);
@@ -256,52 +290,103 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             };
             auto issue_pv = [&](int i, int slot, uint32_t acc) {
                 const uint64_t vd = v_desc + (uint64_t)slot * kTileStep;
-                const uint32_t to = tmem + Lay::col_o(i), ts = tmem + Lay::col_s(i);
+                const uint32_t to = tmem + Lay::col_o(i), tp = tmem + Lay::col_p(i);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                    ptx::mma_ts(to, ts + k * 8, vd + (uint64_t)((k * 2048) >> 4), idesc_pv, (acc | (uint32_t)k) != 0);
+                    ptx::mma_ts(to, tp + k * 8, vd + (uint64_t)((k * 2048) >> 4), idesc_pv, (acc | (uint32_t)k) != 0);
             };
 
-            bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
-                      wait_bounded(&pair_full[0], 0, p.wait_limit_ns, kSiteSlotFull, ab);
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_s(0, 0);
-                ptx::mma_commit(&s_full[0]);
-                issue_s(1, 0);
-                ptx::mma_commit(&s_full[1]);
-                ptx::mma_commit(&pair_empty[0]);      // K_0 is read
-            }
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int slot_v = (2 * j + 1) % Lay::kSlots, slot_k = (2 * j + 2) % Lay::kSlots;
-                const bool more = (j + 1 < n_kv);
-                // pair j+1: V_j, and K_{j+1} when there is a next block
-                if (!wait_bounded(&pair_full[(j + 1) % Lay::kPairs], ((j + 1) / Lay::kPairs) & 1,
-                                  p.wait_limit_ns, kSiteSlotFull, ab) ||
-                    !wait_bounded(&p_full[0], j & 1, p.wait_limit_ns, kSitePFull, ab))
-                    break;
-                ptx::tc_fence_after();
-                issue_pv(0, slot_v, j > 0);
-                if (!more) ptx::mma_commit(&o_final[0]);
-                if (more) {
-                    issue_s(0, slot_k);
+            if constexpr (!Lay::kPApart) {
+                bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
+                          wait_bounded(&pair_full[0], 0, p.wait_limit_ns, kSiteSlotFull, ab);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(0, 0);
                     ptx::mma_commit(&s_full[0]);
-                }
-                if (!wait_bounded(&p_full[1], j & 1, p.wait_limit_ns, kSitePFull, ab)) break;
-                ptx::tc_fence_after();
-                issue_pv(1, slot_v, j > 0);
-                if (!more) ptx::mma_commit(&o_final[1]);
-                if (more) {
-                    issue_s(1, slot_k);
+                    issue_s(1, 0);
                     ptx::mma_commit(&s_full[1]);
+                    ptx::mma_commit(&pair_empty[0]);      // K_0 is read
                 }
-                ptx::mma_commit(&pair_empty[(j + 1) % Lay::kPairs]);   // V_j and K_{j+1} are read
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const int slot_v = (2 * j + 1) % Lay::kSlots, slot_k = (2 * j + 2) % Lay::kSlots;
+                    const bool more = (j + 1 < n_kv);
+                    // pair j+1: V_j, and K_{j+1} when there is a next block
+                    if (!wait_bounded(&pair_full[(j + 1) % Lay::kPairs], ((j + 1) / Lay::kPairs) & 1,
+                                      p.wait_limit_ns, kSiteSlotFull, ab) ||
+                        !wait_bounded(&p_full[0], j & 1, p.wait_limit_ns, kSitePFull, ab))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_pv(0, slot_v, j > 0);
+                    if (!more) ptx::mma_commit(&o_final[0]);
+                    if (more) {
+                        issue_s(0, slot_k);
+                        ptx::mma_commit(&s_full[0]);
+                    }
+                    if (!wait_bounded(&p_full[1], j & 1, p.wait_limit_ns, kSitePFull, ab)) break;
+                    ptx::tc_fence_after();
+                    issue_pv(1, slot_v, j > 0);
+                    if (!more) ptx::mma_commit(&o_final[1]);
+                    if (more) {
+                        issue_s(1, slot_k);
+                        ptx::mma_commit(&s_full[1]);
+                    }
+                    ptx::mma_commit(&pair_empty[(j + 1) % Lay::kPairs]);   // V_j and K_{j+1} are read
+                }
+            } else if (warp == 1) {
+                // PV products.  Pair 0 (K_0 alone) has nothing for them.
+                ptx::mma_commit(&pair_empty[0]);
+                for (int j = 0; j < n_kv; ++j) {
+                    const int slot_v = (2 * j + 1) % Lay::kSlots;
+                    bool ok = wait_bounded(&pair_full[(j + 1) % Lay::kPairs], ((j + 1) / Lay::kPairs) & 1,
+                                           p.wait_limit_ns, kSiteSlotFull, ab);
+                    for (int i = 0; i < 2 && ok; ++i) {
+                        ok = wait_bounded(&p_full[i], j & 1, p.wait_limit_ns, kSitePFull, ab);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_pv(i, slot_v, j > 0);
+                        ptx::mma_commit(&pv_done[i]);
+                        if (j + 1 == n_kv) ptx::mma_commit(&o_final[i]);
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(&pair_empty[(j + 1) % Lay::kPairs]);   // V_j is read
+                }
+            } else {
+                // S products: S_i(j+1) may overwrite S_i(j) as soon as tile
+                // i's softmax warps hold S_i(j) in registers, so it is
+                // computed while they work on block j.
+                bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) &&
+                          wait_bounded(&pair_full[0], 0, p.wait_limit_ns, kSiteSlotFull, ab);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(0, 0);
+                    ptx::mma_commit(&s_full[0]);
+                    issue_s(1, 0);
+                    ptx::mma_commit(&s_full[1]);
+                    ptx::mma_commit(&pair_empty[0]);      // K_0 is read
+                }
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    if (j + 1 < n_kv) {
+                        const int slot_k = (2 * j + 2) % Lay::kSlots;
+                        ok = wait_bounded(&pair_full[(j + 1) % Lay::kPairs], ((j + 1) / Lay::kPairs) & 1,
+                                          p.wait_limit_ns, kSiteSlotFull, ab);
+                        for (int i = 0; i < 2 && ok; ++i) {
+                            ok = wait_bounded(&s_read[i], j & 1, p.wait_limit_ns, kSiteSFull, ab);
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            issue_s(i, slot_k);
+                            ptx::mma_commit(&s_full[i]);
+                        }
+                        if (!ok) break;
+                    }
+                    ptx::mma_commit(&pair_empty[(j + 1) % Lay::kPairs]);   // K_{j+1} is read
+                }
             }
             // Drain: every MMA this thread issued is complete before TMEM is
             // freed (on the normal path o_final already covered them; after an
             // abort some may still be in flight).
-            ptx::mma_commit(mma_drain);
-            wait_bounded(mma_drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
+            uint64_t *drain = (Lay::kPApart && warp == 3) ? mma_drain_s : mma_drain;
+            ptx::mma_commit(drain);
+            wait_bounded(drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
         }
     }
     } else {
@@ -314,6 +399,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + Lay::col_s(i);
         const uint32_t tO = tmem + lane_off + Lay::col_o(i);
+        const uint32_t tP = tmem + lane_off + Lay::col_p(i);
         const int64_t lim = p.causal ? (L < row + 1 ? L : row + 1) : L;   // visible keys: j < lim
         const float sl2 = p.scale_log2;
 
@@ -330,6 +416,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s_raw[c]);
             ptx::tmem_wait_ld();
+            if constexpr (Lay::kPApart) {
+                // S_i(j) is in registers: its columns are free for S_i(j+1)
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&s_read[i]);
+            }
 
             const int64_t vis = lim - (int64_t)(blk0 + j) * BN;   // columns k < vis are visible
             if (vis < BN) {
@@ -339,9 +431,24 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int t = 0; t < 32; ++t)
                         if (c * 32 + t >= vis) s_raw[c][t] = f2u(-INFINITY);
             }
-            // O_i is never being written here: s_full[i] for block j is
-            // committed after PV_i of block j-1.
-            st.block(s_raw, sl2, j > 0, tS, tO, [] {});
+            if constexpr (!Lay::kPApart) {
+                // O_i is never being written here: s_full[i] for block j is
+                // committed after PV_i of block j-1.
+                st.block(s_raw, sl2, j > 0, tP, tO, [] {});
+            } else {
+                // PV_i(j-1) runs on the other MMA thread and may still read
+                // P_i and write O_i: it has to end before the first P store
+                // and before any access to O.
+                auto pv_prev = [&] {
+                    if (j > 0) {
+                        const bool done = wait_bounded(&pv_done[i], (j - 1) & 1, p.wait_limit_ns, kSitePFull, ab);
+                        if (!__all_sync(0xffffffffu, done)) ok = false;
+                        ptx::tc_fence_after();
+                    }
+                };
+                st.block<kEarlyChunks>(s_raw, sl2, j > 0, tP, tO, pv_prev, pv_prev);
+                if (!ok) break;
+            }
             // every lane's P stores have landed (block() waited for them);
             // after the warp has synchronised, one lane tells the MMA warp
             ptx::tc_fence_before();

@@ -9,12 +9,13 @@
 //   * one CTA owns one 128-row query tile; TMEM holds two score tiles S_a,
 //     S_b (128 columns each), O (D columns) and, for D <= 128, two P tiles of
 //     their own (64 columns each: 16-bit pairs);
-//   * warp 1 issues the MMAs in the order S_0, S_1, then per key block j:
-//     O += P_j V_j and S_{j+2} = Q K_{j+2}^T into the score tile S_j has
-//     left.  The tensor core so holds the next block's scores ready while
-//     warps 4-7 run the softmax of this one, and the softmax never waits for
-//     the products that follow it: with P apart from S, S_{j+2} may be
-//     computed as soon as the softmax of block j has read S_j;
+//   * with P apart (D <= 128) warp 3 issues S_0, S_1 and then S_{j+2} =
+//     Q K_{j+2}^T into the score tile of S_j as soon as the softmax warps
+//     hold S_j in registers, and warp 1 issues O += P_j V_j once they hand
+//     P_j over.  The tensor core so holds the next block's scores ready while
+//     warps 4-7 run the softmax of this one, and two issuing threads keep it
+//     busier than one (one thread issues at most one N=128 product per
+//     ~90-100 clk on this GPU, two reach the 64 clk rate);
 //   * warp 0 streams K and V through rings of kRing slots each, in the order
 //     the MMAs read them (K_0, K_1, V_0, K_2, V_1, ...), so a load has several
 //     blocks' time to land;
@@ -24,8 +25,10 @@
 // O is rescaled in TMEM only when the lazy reference max moves; because
 // O += P_{j-1} V_{j-1} may still be running when the softmax of block j
 // starts, such a rescale first waits for that product.  P tile j % 2 is free
-// for block j once S_j is complete: S_j is issued after O += P_{j-2} V_{j-2},
-// the last reader of that tile, and its commit covers every earlier MMA.
+// for block j once O += P_{j-2} V_{j-2}, its last reader, is done: with P
+// apart the softmax waits for that product's commit before its first P
+// store; with P over S (D = 256) the commit that completed S_j covers it,
+// because one thread issued S_j after it.
 //
 // Every mbarrier wait is bounded; a wait that runs out records the site in
 // this file's status word, raises the CTA's abort flag, and every role drains
@@ -45,7 +48,7 @@ namespace {
 
 constexpr int BM = 128;                         // query rows per CTA (= TMEM lanes)
 constexpr int BN = 128;                         // keys per block
-constexpr int kThreads = 256;                   // warp 0 TMA, warp 1 MMA, warps 4-7 softmax
+constexpr int kThreads = 256;                   // warp 0 TMA, warps 1 and 3 MMA, warps 4-7 softmax
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kChunkBytes = 128 * 128;          // one 128-row x 64-column 16-bit box
 constexpr uint32_t kTmemCols = 512;
@@ -63,7 +66,7 @@ struct OneTileLayout {
     static constexpr int kKOff = kTileBytes;                        // K slots
     static constexpr int kVOff = kKOff + kRing * kTileBytes;        // V slots
     static constexpr int kBarOff = kVOff + kRing * kTileBytes;
-    static constexpr int kBars = 1 + 4 * kRing + 9;
+    static constexpr int kBars = 1 + 4 * kRing + 12;
     // At least 120 KB, so that one CTA (and its 512 TMEM columns) sits on an SM.
     static constexpr int kNeed = kBarOff + 256 + 1024;      // + alignment slack
     static constexpr int kSmemBytes = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
@@ -103,6 +106,10 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint64_t *pv_done = p_full + 2;            // [2], per P tile: O += P V has read it
     uint64_t *o_final = pv_done + 2;
     uint64_t *mma_drain = o_final + 1;
+    // P apart only: score tile read into the softmax warps' registers (it may
+    // be overwritten), and the drain of the second MMA thread.
+    uint64_t *s_read = mma_drain + 1;          // [2], per score tile
+    uint64_t *mma_drain_s = s_read + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Lay::kBars);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     const Abort ab{abort_word, &g_status_onetile};
@@ -128,7 +135,8 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (threadIdx.x == 0) {
         // P hand-offs take one arrival per softmax warp, the rest one
         for (int i = 0; i < Lay::kBars; ++i)
-            ptx::mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? 4 : 1);
+            ptx::mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1] || &bars[i] == &s_read[0] ||
+                                      &bars[i] == &s_read[1]) ? 4 : 1);
         *abort_word = 0;
         ptx::fence_mbarrier_init();
         // Thread 0 is also the producer: Q and K_0 are requested now, so that
@@ -200,8 +208,14 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int t = v_issued > R ? v_issued - R : 0; t < v_issued; ++t)
                 wait_bounded(&v_full[t % R], (t / R) & 1, p.wait_limit_ns, kSiteDrain, ab, false);
         }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
+    } else if (warp == 1 || (Lay::kPApart && warp == 3)) {
+        // ================= MMA issuers =================
+        // With P apart (D <= 128) warp 1 issues the PV products and warp 3
+        // the S products: the two streams touch disjoint TMEM columns, and
+        // two issuing threads keep the tensor core busier than one (a probe
+        // on this GPU ran one thread's N=128 products at ~110 clk each, two
+        // threads' at ~70 clk per product together).  At D = 256 (P over S)
+        // warp 1 issues both, S_{j+1} behind the PV that reads its columns.
         if (lane == 0 && n_kv > 0) {
             constexpr uint32_t idesc_qk = make_idesc(BM, BN, 0, 0, kF16);
             constexpr uint32_t idesc_pv = make_idesc(BM, D, 0, 1, kF16);
@@ -239,29 +253,50 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 ptx::mma_commit(&k_empty[t % R]);
                 return true;
             };
-            bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) && next_s(0);
-            // P apart from S: both score tiles are free at the start.
-            if (ok && Lay::kPApart && n_kv > 1) ok = next_s(1);
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int buf = j & 1;
-                // P over S: S_{j+1} goes into the score tile P_{j-1} has left,
-                // after O += P_{j-1} V_{j-1} (issued before it, so read before).
-                if (!Lay::kPApart && j + 1 < n_kv && !next_s(j + 1)) break;
-                if (!wait_bounded(&v_full[j % R], (j / R) & 1, p.wait_limit_ns, kSiteSlotFull, ab) ||
-                    !wait_bounded(&p_full[buf], (j >> 1) & 1, p.wait_limit_ns, kSitePFull, ab))
-                    break;
-                ptx::tc_fence_after();
-                issue_pv(buf, j % R, j > 0);
-                ptx::mma_commit(&v_empty[j % R]);
-                ptx::mma_commit(&pv_done[buf]);
-                if (j + 1 == n_kv) ptx::mma_commit(o_final);
-                // P apart: S_{j+2} into the score tile the softmax of block j
-                // has read (it handed P_j over after reading S_j).
-                if (Lay::kPApart && j + 2 < n_kv && !next_s(j + 2)) break;
+            if constexpr (!Lay::kPApart) {
+                bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) && next_s(0);
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const int buf = j & 1;
+                    // P over S: S_{j+1} goes into the score tile P_{j-1} has
+                    // left, after O += P_{j-1} V_{j-1} (issued before it, so
+                    // read before).
+                    if (j + 1 < n_kv && !next_s(j + 1)) break;
+                    if (!wait_bounded(&v_full[j % R], (j / R) & 1, p.wait_limit_ns, kSiteSlotFull, ab) ||
+                        !wait_bounded(&p_full[buf], (j >> 1) & 1, p.wait_limit_ns, kSitePFull, ab))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_pv(buf, j % R, j > 0);
+                    ptx::mma_commit(&v_empty[j % R]);
+                    ptx::mma_commit(&pv_done[buf]);
+                    if (j + 1 == n_kv) ptx::mma_commit(o_final);
+                }
+            } else if (warp == 1) {
+                // PV products: O += P_j V_j once the softmax has handed P_j over.
+                for (int j = 0; j < n_kv; ++j) {
+                    const int buf = j & 1;
+                    if (!wait_bounded(&v_full[j % R], (j / R) & 1, p.wait_limit_ns, kSiteSlotFull, ab) ||
+                        !wait_bounded(&p_full[buf], (j >> 1) & 1, p.wait_limit_ns, kSitePFull, ab))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_pv(buf, j % R, j > 0);
+                    ptx::mma_commit(&v_empty[j % R]);
+                    ptx::mma_commit(&pv_done[buf]);
+                    if (j + 1 == n_kv) ptx::mma_commit(o_final);
+                }
+            } else {
+                // S products: S_0 and S_1 into the two score tiles, then S_t
+                // into tile t % 2 as soon as the softmax warps hold S_{t-2}
+                // in registers.
+                bool ok = wait_bounded(q_full, 0, p.wait_limit_ns, kSiteQFull, ab) && next_s(0);
+                if (ok && n_kv > 1) ok = next_s(1);
+                for (int t = 2; t < n_kv && ok; ++t)
+                    ok = wait_bounded(&s_read[t & 1], ((t - 2) >> 1) & 1, p.wait_limit_ns, kSiteSFull, ab) &&
+                         next_s(t);
             }
             // Drain: every MMA issued here completes before TMEM is freed.
-            ptx::mma_commit(mma_drain);
-            wait_bounded(mma_drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
+            uint64_t *drain = (Lay::kPApart && warp == 3) ? mma_drain_s : mma_drain;
+            ptx::mma_commit(drain);
+            wait_bounded(drain, 0, p.wait_limit_ns, kSiteDrain, ab, false);
         }
     } else if (warp >= kSoftmaxWarp0) {
         // ================= online softmax + epilogue =================
@@ -284,14 +319,17 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 ok = false;
                 break;
             }
-            // P tile `buf` was last read by O += P_{j-2} V_{j-2}.  S_j was
-            // issued after that product, and the commit that completed S_j
-            // covers every earlier op of the MMA thread, so the tile is free.
             ptx::tc_fence_after();
             uint32_t s_raw[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s_raw[c]);
             ptx::tmem_wait_ld();
+            if constexpr (Lay::kPApart) {
+                // S_j is in registers: its tile is free for S_{j+2}
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&s_read[buf]);
+            }
             const int64_t vis = lim - (int64_t)j * BN;   // columns k < vis are visible
             if (vis < BN) {
 #pragma unroll
@@ -301,12 +339,25 @@ fwd_onetile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         if (c * 32 + t >= vis) s_raw[c][t] = f2u(-INFINITY);
             }
             // O += P_{j-1} V_{j-1} may still be running: an O rescale waits
-            // for it first.
+            // for it first.  P tile `buf` was last read by O += P_{j-2}
+            // V_{j-2}.  With P over S (D = 256), S_j was issued after that
+            // product by the same thread, so the commit that completed S_j
+            // covers it; with P apart, the PV thread's own commit is waited
+            // for before the first P store.
             bool hook_ok = true;
-            st.block(s_raw, sl2, j > 0, tP, tO, [&] {
-                hook_ok = wait_bounded(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.wait_limit_ns, kSiteOFinal, ab);
+            auto before_o = [&] {
+                hook_ok = wait_bounded(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.wait_limit_ns, kSiteOFinal,
+                                       ab) && hook_ok;
                 ptx::tc_fence_after();
-            });
+            };
+            auto before_p = [&] {
+                if (Lay::kPApart && j >= 2) {
+                    hook_ok = wait_bounded(&pv_done[buf], ((j - 2) >> 1) & 1, p.wait_limit_ns, kSiteOFinal, ab) &&
+                              hook_ok;
+                    ptx::tc_fence_after();
+                }
+            };
+            st.block(s_raw, sl2, j > 0, tP, tO, before_o, before_p);
             // every lane's P stores have landed; after the warp has
             // synchronised, one lane tells the MMA warp
             ptx::tc_fence_before();

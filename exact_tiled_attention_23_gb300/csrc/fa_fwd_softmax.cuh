@@ -98,10 +98,15 @@ struct OnlineRow {
 
     // p = 2^(S*scale*log2e - m_ref): packed FMA, MUFU ex2, packed sums; P
     // goes to the 64 columns at tP as 16-bit pairs.  Returns sum p in `sum`
-    // and the sum of the stored (rounded) P in `sum_o`.
+    // and the sum of the stored (rounded) P in `sum_o`.  pre_store() runs
+    // (warp-uniformly) once the first kEarly x 32 scores are done, before the
+    // first P store: a kernel whose P columns may still be read by the
+    // previous product waits for it there, with that much of the pass done.
+    template <int kEarly, typename PreStore>
     __device__ __forceinline__ void exp_pass(const uint32_t (&s)[4][32], float sl2, uint32_t tP, float &sum,
-                                             float &sum_o) const
+                                             float &sum_o, PreStore &pre_store) const
     {
+        static_assert(kEarly >= 1 && kEarly <= 4, "chunks before the first P store");
         const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const uint64_t t2 = ptx::pack2(sl2, sl2);
         const uint64_t nm2 = ptx::pack2(-mref_use, -mref_use);
@@ -111,8 +116,9 @@ struct OnlineRow {
 #pragma unroll
         for (int a = 0; a < 2; ++a) rnd2[a] = 0ull;
 #pragma unroll
+        uint32_t pk[4][16];
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 float y0, y1;
@@ -120,10 +126,16 @@ struct OnlineRow {
                 const float p0 = ptx::ex2_approx(y0);
                 const float p1 = ptx::ex2_approx(y1);
                 acc2[t & 3] = ptx::add2(acc2[t & 3], ptx::pack2(p0, p1));
-                pk[t] = ptx::pack16x2<kF16>(p0, p1);
-                rnd2[t & 1] = ptx::add2(rnd2[t & 1], ptx::widen16x2<kF16>(pk[t]));
+                pk[c][t] = ptx::pack16x2<kF16>(p0, p1);
+                rnd2[t & 1] = ptx::add2(rnd2[t & 1], ptx::widen16x2<kF16>(pk[c][t]));
             }
-            ptx::tmem_st16(tP + c * 16, pk);
+            if (c + 1 == kEarly) {
+                pre_store();
+#pragma unroll
+                for (int e = 0; e <= c; ++e) ptx::tmem_st16(tP + e * 16, pk[e]);
+            } else if (c >= kEarly) {
+                ptx::tmem_st16(tP + c * 16, pk[c]);
+            }
         }
         float a0, a1, b0, b1, c0, c1, d0, d1;
         ptx::unpack2(acc2[0], a0, a1);
@@ -138,23 +150,34 @@ struct OnlineRow {
 
     // One key block; P goes to tP.  o_live: O at tO holds earlier blocks.
     // before_o_touch() runs (warp-uniformly) before any access to O, for
-    // kernels whose O may still be written by an MMA at that point.  On
+    // kernels whose O may still be written by an MMA at that point;
+    // before_p_store() before the first store to tP, for kernels whose P
+    // columns may still be read by one (both may run more than once).  On
     // return every P store has landed in TMEM.
-    template <typename Hook>
+    // kEarly: chunks of 32 scores exponentiated before before_p_store() and
+    // the first P store.
+    template <int kEarly = 1, typename Hook, typename PreStore>
     __device__ __forceinline__ void block(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tP,
-                                          uint32_t tO, Hook &&before_o_touch)
+                                          uint32_t tO, Hook &&before_o_touch, PreStore &&before_p_store)
     {
         if (__any_sync(0xffffffffu, m_ref == -INFINITY)) raise(s, sl2, o_live, tO, before_o_touch);
         float sum, sum_o;
-        exp_pass(s, sl2, tP, sum, sum_o);
+        exp_pass<kEarly>(s, sl2, tP, sum, sum_o, before_p_store);
         if (__any_sync(0xffffffffu, !(sum <= (kF16 ? kLazyLimitF16 : kLazyLimit)))) {
             raise(s, sl2, o_live, tO, before_o_touch);
             ptx::tmem_wait_st();      // the first pass's P stores land before the new ones
-            exp_pass(s, sl2, tP, sum, sum_o);
+            exp_pass<kEarly>(s, sl2, tP, sum, sum_o, before_p_store);
         }
         ptx::tmem_wait_st();
         l += sum;
         l_o += sum_o;
+    }
+
+    template <typename Hook>
+    __device__ __forceinline__ void block(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tP,
+                                          uint32_t tO, Hook &&before_o_touch)
+    {
+        block<1>(s, sl2, o_live, tP, tO, before_o_touch, [] {});
     }
 };
 
