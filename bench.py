@@ -86,6 +86,8 @@ KERNEL_SOURCES = {
     "fwd_fp32_kernel": ("fa_fwd_fp32.cu", "fa_internal.h", "fa_api.cu"),
     "fwd_onetile_kernel": ("fa_fwd_onetile.cu", "fa_fwd_softmax.cuh", "fa_tc_common.cuh", "sm103_ptx.cuh",
                            "fa_internal.h", "fa_api.cu"),
+    "fwd_halves_kernel": ("fa_fwd_halves.cu", "fa_fwd_softmax.cuh", "fa_tc_common.cuh", "sm103_ptx.cuh",
+                          "fa_internal.h", "fa_api.cu"),
 }
 
 
@@ -447,14 +449,11 @@ def run_ours(args, rank, world, local):
     if w.dtype in ("bf16", "fp16"):
         # fp16 and bf16 have the same dense tensor rate (kind::f16)
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
-        # the library runs one 128-row query tile per CTA for D = 256 and for
-        # grids whose one-tile CTAs fit in one wave (FA_FWD_TILES forces it)
-        items = B * H * ((N + 255) // 256)
-        forced = os.environ.get("FA_FWD_TILES", "")
-        one_tile = D == 256 or forced == "1" or (
-            forced != "2" and 2 * items <= torch.cuda.get_device_properties(dev).multi_processor_count)
+        # the kernel the library runs for these sizes (FA_FWD_TILES forces one)
+        choice = fa.fa_fwd_kernel_choice(B, H, N, D)
         kname = ("bwd_kernel" if args.pass_ == "bwd" else
-                 "fwd_onetile_kernel" if splits is None and one_tile else "fwd_bf16_kernel")
+                 "fwd_bf16_kernel" if splits is not None else
+                 {1: "fwd_onetile_kernel", 3: "fwd_halves_kernel"}.get(choice, "fwd_bf16_kernel"))
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": profiled_traffic(w.name, kname),
                     "peak_kind": f"{peak_kind} dense bf16 (burst)",

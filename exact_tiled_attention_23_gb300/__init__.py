@@ -26,7 +26,7 @@ from . import _build
 __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FAError", "load", "library_path", "fa_fwd", "fa_fwd_fp32", "fa_status_string",
            "fa_device_status", "fa_last_error_detail", "fa_fwd_splitkv",
-           "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "FA_MAX_SPLITS",
+           "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_auto_splits", "fa_fwd_kernel_choice", "FA_MAX_SPLITS",
            "fa_fwd_splitkv_noalloc", "FA_NOALLOC_SCRATCH_BYTES", "fa_fwd_f16",
            "fa_bwd", "fa_bwd_f16", "fa_bwd_workspace_bytes", "backward", "attention",
            "fa_fwd_from_host", "fa_fwd_from_host_auto_groups", "FA_MAX_HOST_GROUPS", "forward_from_host",
@@ -92,6 +92,8 @@ def load():
         lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_splitkv_auto_splits.argtypes = [i32, i32, i32, i32]
         lib.fa_fwd_splitkv_auto_splits.restype = i32
+        lib.fa_fwd_kernel_choice.argtypes = [i32, i32, i32, i32]
+        lib.fa_fwd_kernel_choice.restype = i32
         lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp,
                                                i32, vp]
         lib.fa_fwd_splitkv_noalloc.restype = i32
@@ -184,6 +186,10 @@ def fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits) -> int:
 
 def fa_fwd_splitkv_auto_splits(B, H, N, D) -> int:
     return int(load().fa_fwd_splitkv_auto_splits(B, H, N, D))
+
+
+def fa_fwd_kernel_choice(B, H, N, D) -> int:
+    return int(load().fa_fwd_kernel_choice(B, H, N, D))
 
 
 def fa_status_string(status: int) -> str:

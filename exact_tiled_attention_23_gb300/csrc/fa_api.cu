@@ -50,15 +50,15 @@ uint64_t wait_limit_ns()
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Query tiles per CTA of the tensor-core forward that FA_FWD_TILES asks for:
-// "1" or "2", else 0 (the automatic choice).  Read on every call, so that a
-// process can compare the two kernels.
+// The tensor-core forward kernel that FA_FWD_TILES asks for: "1" (one query
+// tile per CTA), "2" (two tiles per CTA) or "3" (one tile, split rows), else
+// 0 (the automatic choice).  Read on every call, so that a process can
+// compare the kernels.
 int forced_tiles()
 {
     const char *e = std::getenv("FA_FWD_TILES");
     if (!e) return 0;
-    if (e[0] == '1' && e[1] == 0) return 1;
-    if (e[0] == '2' && e[1] == 0) return 2;
+    if (e[0] >= '1' && e[0] <= '3' && e[1] == 0) return e[0] - '0';
     return 0;
 }
 
@@ -159,19 +159,28 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, in
     return encode_map16(m, base, BH, N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-// Query tiles per CTA of the kernel the tensor-core forward runs for a
-// problem: the two-tile kernel's work item covers 256 query rows of one head;
-// the one-tile kernel's covers 128 and runs D = 256, and grids whose twice as
-// many one-tile CTAs still fit in one wave (one CTA per SM).
+// The kernel the tensor-core forward runs for a problem (measured on GB300):
+//   1: one 128-row query tile per CTA -- D = 256, and grids of D <= 64 whose
+//      twice as many one-tile CTAs still fit in one wave (one CTA per SM);
+//   3: one tile per CTA, each row's keys split between two softmax
+//      warpgroups -- 64 < D <= 128 with long rows (N >= 8192), where it runs
+//      ahead of the two-tile kernel, or with such small grids;
+//   2: two tiles per CTA (work item: 256 query rows of one head) otherwise,
+//      where it runs ahead: D <= 64, and shorter rows (whose per-tile ramp the
+//      two-tile kernel amortises over twice the rows).
 int choose_tiles(int B, int H, int N, int D)
 {
     const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
     const int forced = forced_tiles();
-    return (D == 256 || forced == 1 || (forced == 0 && 2 * items <= sm_count())) ? 1 : 2;
+    if (D == 256) return 1;
+    if (forced != 0) return forced;
+    const bool small_grid = 2 * items <= sm_count();
+    if (D > 64) return (small_grid || N >= 8192) ? 3 : 2;
+    return small_grid ? 1 : 2;
 }
 
 // Shared checks and launch of the single-pass tensor-core kernel.  tiles: the
-// kernel (1 or 2), or 0 for choose_tiles on this call's sizes.
+// kernel (1, 2 or 3), or 0 for choose_tiles on this call's sizes.
 fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                 int N, int D, int causal, float scale, const int32_t *kv_len, void *stream, bool f16,
                 int tiles = 0)
@@ -184,8 +193,8 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
     if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_INVALID_ARG;
     if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
     if (tiles == 0) tiles = choose_tiles(B, H, N, D);
-    if ((tiles != 1 && tiles != 2) || (tiles == 2 && D == 256)) return FA_ERR_INVALID_ARG;
-    const bool one_tile = tiles == 1;
+    if (tiles < 1 || tiles > 3 || (tiles != 1 && D == 256)) return FA_ERR_INVALID_ARG;
+    const bool one_tile = tiles != 2;
     // The grid is 1-D.
     const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
     const int64_t ctas = one_tile ? (int64_t)B * H * (((int64_t)N + 127) / 128) : items;
@@ -198,8 +207,10 @@ fa_status fwd16(const void *Q, const void *K, const void *V, void *O, float *LSE
         return FA_ERR_CUDA;
     fa::FwdParams p = make_params(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len);
     p.f16 = f16 ? 1 : 0;
-    cudaError_t e = one_tile ? fa::launch_fwd_onetile(p, tq, tk, tv, to, static_cast<cudaStream_t>(stream))
-                             : fa::launch_fwd_bf16(p, tq, tk, tv, to, static_cast<cudaStream_t>(stream));
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = tiles == 1   ? fa::launch_fwd_onetile(p, tq, tk, tv, to, cs)
+                    : tiles == 3 ? fa::launch_fwd_halves(p, tq, tk, tv, to, cs)
+                                 : fa::launch_fwd_bf16(p, tq, tk, tv, to, cs);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -290,6 +301,12 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits
     if (B < 0 || H < 0 || N < 0 || D <= 0 || num_splits < 0 || num_splits > FA_MAX_SPLITS) return 0;
     if (num_splits == 0) num_splits = fa_fwd_splitkv_auto_splits(B, H, N, D);
     return (size_t)num_splits * (size_t)B * (size_t)H * (size_t)N * ((size_t)D + 1) * sizeof(float);
+}
+
+int fa_fwd_kernel_choice(int B, int H, int N, int D)
+{
+    if (!tc_fwd_head_dim(D) && D != 256) return 0;
+    return choose_tiles(B < 0 ? 0 : B, H < 0 ? 0 : H, N < 0 ? 0 : N, D);
 }
 
 int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D)
@@ -395,11 +412,12 @@ const char *fa_status_string(fa_status s)
 
 fa_status fa_device_status(void *stream)
 {
-    uint32_t v = 0, vb = 0, vd = 0;
+    uint32_t v = 0, vb = 0, vd = 0, vh = 0;
     if (fa::read_and_clear_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess ||
-        fa::read_and_clear_status_bwd(&vb) != cudaSuccess || fa::read_and_clear_status_onetile(&vd) != cudaSuccess)
+        fa::read_and_clear_status_bwd(&vb) != cudaSuccess || fa::read_and_clear_status_onetile(&vd) != cudaSuccess ||
+        fa::read_and_clear_status_halves(&vh) != cudaSuccess)
         return FA_ERR_CUDA;
-    v |= vb | vd;
+    v |= vb | vd | vh;
     if (v) {
         g_last_detail = v;
         if (v & fa::kStatusTimeout) return FA_ERR_TIMEOUT;

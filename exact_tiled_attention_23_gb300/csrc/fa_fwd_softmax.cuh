@@ -1,12 +1,12 @@
 // fa_fwd_softmax.cuh -- the online-softmax step of one query row over one key
-// block of 128 scores, shared by the tensor-core forward kernels.
+// block of 128 (or 64) scores, shared by the tensor-core forward kernels.
 //
-// One thread owns one query row (one TMEM lane).  Per key block it has the
-// row's 128 raw scores S = q.k in registers (fp32 bits, masked entries
-// already -inf) and turns them into P = 2^(S*scale*log2e - m_ref), stored as
-// 16-bit pairs in 64 TMEM columns (over the first 64 columns of the score
-// tile, or in columns of their own), while keeping the running sum l against
-// the same reference m_ref.  This is the
+// One thread owns one query row (one TMEM lane), or one half of a row's keys.
+// Per key block it has its kCols raw scores S = q.k in registers (fp32 bits,
+// masked entries already -inf) and turns them into P = 2^(S*scale*log2e -
+// m_ref), stored as 16-bit pairs in kCols/2 TMEM columns (over the first
+// columns of the score tile, or in columns of their own), while keeping the
+// running sum l against the same reference m_ref.  This is the
 // recurrence of "vectorized-flash-attention-kernel", Core algorithm step 3,
 // in base 2.
 //
@@ -42,9 +42,13 @@ constexpr float kLazyLimit = 18446744073709551616.f;
 // With fp16 operands P must also fit fp16 (max 65504): every p <= 2^15.
 constexpr float kLazyLimitF16 = 32768.f;
 
-// D: number of fp32 O columns in TMEM for this row; kF16: P is fp16 (else bf16).
-template <int D, bool kF16>
+// D: number of fp32 O columns in TMEM for this row; kF16: P is fp16 (else
+// bf16); kCols: scores per key block (128, or 64 when two threads share a row
+// and each keeps its own m_ref, l, l_o and O).
+template <int D, bool kF16, int kCols = 128>
 struct OnlineRow {
+    static_assert(kCols == 64 || kCols == 128, "scores per block");
+    static constexpr int kC = kCols / 32;      // 32-score chunks
     float m_ref = -INFINITY;   // reference max of scale*log2e*S: a lower bound of the running max
     float l = 0.f;             // running sum of p against m_ref (fp32 p): the LSE
     float l_o = 0.f;           // running sum of the 16-bit rounded P: O's normaliser
@@ -53,22 +57,22 @@ struct OnlineRow {
     // already holds earlier blocks) by 2^(m_old - m_new).  before_o_touch()
     // runs, warp-uniformly, just before O is read.
     template <typename Hook>
-    __device__ __forceinline__ void raise(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tO,
+    __device__ __forceinline__ void raise(const uint32_t (&s)[kC][32], float sl2, bool o_live, uint32_t tO,
                                           Hook &before_o_touch)
     {
-        // Eight running maxima: scores 0..7, then 16 per step over 8..119
-        // (two per 3-input max), then 120..127.
+        // Eight running maxima: scores 0..7, then 16 per step over
+        // 8..kCols-9 (two per 3-input max), then the last 8.
         float mx8[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx8[a] = u2f(s[0][a]);
 #pragma unroll
-        for (int k = 8; k < 120; k += 16)
+        for (int k = 8; k < kCols - 8; k += 16)
 #pragma unroll
             for (int a = 0; a < 8; ++a)
                 mx8[a] = ptx::max3(mx8[a], u2f(s[(k + 2 * a) / 32][(k + 2 * a) % 32]),
                                    u2f(s[(k + 2 * a + 1) / 32][(k + 2 * a + 1) % 32]));
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(mx8[a], u2f(s[3][24 + a]));
+        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(mx8[a], u2f(s[kC - 1][24 + a]));
         const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
                                fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_ref, mx * sl2);
@@ -103,10 +107,10 @@ struct OnlineRow {
     // first P store: a kernel whose P columns may still be read by the
     // previous product waits for it there, with that much of the pass done.
     template <int kEarly, typename PreStore>
-    __device__ __forceinline__ void exp_pass(const uint32_t (&s)[4][32], float sl2, uint32_t tP, float &sum,
+    __device__ __forceinline__ void exp_pass(const uint32_t (&s)[kC][32], float sl2, uint32_t tP, float &sum,
                                              float &sum_o, PreStore &pre_store) const
     {
-        static_assert(kEarly >= 1 && kEarly <= 4, "chunks before the first P store");
+        static_assert(kEarly >= 1 && kEarly <= kC, "chunks before the first P store");
         const float mref_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const uint64_t t2 = ptx::pack2(sl2, sl2);
         const uint64_t nm2 = ptx::pack2(-mref_use, -mref_use);
@@ -115,10 +119,9 @@ struct OnlineRow {
         for (int a = 0; a < 4; ++a) acc2[a] = 0ull;
 #pragma unroll
         for (int a = 0; a < 2; ++a) rnd2[a] = 0ull;
+        uint32_t pk[kC][16];
 #pragma unroll
-        uint32_t pk[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kC; ++c) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 float y0, y1;
@@ -157,7 +160,7 @@ struct OnlineRow {
     // kEarly: chunks of 32 scores exponentiated before before_p_store() and
     // the first P store.
     template <int kEarly = 1, typename Hook, typename PreStore>
-    __device__ __forceinline__ void block(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tP,
+    __device__ __forceinline__ void block(const uint32_t (&s)[kC][32], float sl2, bool o_live, uint32_t tP,
                                           uint32_t tO, Hook &&before_o_touch, PreStore &&before_p_store)
     {
         if (__any_sync(0xffffffffu, m_ref == -INFINITY)) raise(s, sl2, o_live, tO, before_o_touch);
@@ -174,7 +177,7 @@ struct OnlineRow {
     }
 
     template <typename Hook>
-    __device__ __forceinline__ void block(const uint32_t (&s)[4][32], float sl2, bool o_live, uint32_t tP,
+    __device__ __forceinline__ void block(const uint32_t (&s)[kC][32], float sl2, bool o_live, uint32_t tP,
                                           uint32_t tO, Hook &&before_o_touch)
     {
         block<1>(s, sl2, o_live, tP, tO, before_o_touch, [] {});

@@ -10,13 +10,15 @@
 
 namespace fa {
 
-// The tensor-core forward's kernel for a problem of these sizes (query tiles
-// per CTA: 1 or 2), as fa_fwd / fa_fwd_f16 choose it.
+// The tensor-core forward's kernel for a problem of these sizes, as fa_fwd /
+// fa_fwd_f16 choose it: 1 = one query tile per CTA, 2 = two tiles per CTA,
+// 3 = one tile per CTA with each row's keys split between two softmax
+// warpgroups.
 int fwd16_tiles(int B, int H, int N, int D);
 
-// fa_fwd (f16: fa_fwd_f16) with the kernel fixed by `tiles` (1 or 2), for
+// fa_fwd (f16: fa_fwd_f16) with the kernel fixed by `tiles` (1, 2 or 3), for
 // callers that split one problem into several launches and want every part
-// computed as one whole call would compute it: the two kernels agree only to
+// computed as one whole call would compute it: the kernels agree only to
 // rounding, not bit for bit.
 fa_status fwd16_with_tiles(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                            int N, int D, int causal, float scale, const int32_t *kv_len, bool f16, int tiles,
@@ -60,6 +62,9 @@ struct FwdParams {
     int num_splits;
     float *part_o;
     float *part_lse;
+    // split-row kernel only: heads per group of its CTA order (>= 1; the
+    // launcher sets it)
+    int head_group;
 };
 
 // Arguments of the backward pass (bf16 or fp16 tensors, fp32 LSE and workspace).
@@ -88,6 +93,12 @@ cudaError_t launch_fwd_bf16(const FwdParams &p, const CUtensorMap &tm_q, const C
 cudaError_t launch_fwd_onetile(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t stream);
 
+// One 128-row query tile per CTA, each row's keys split between two softmax
+// warpgroups with separate online-softmax states, merged in the epilogue
+// (D <= 128).
+cudaError_t launch_fwd_halves(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                              const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t stream);
+
 // Split-KV forward: partial kernel over key-block ranges, then the merge.
 cudaError_t launch_fwd_bf16_split(const FwdParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                   const CUtensorMap &tm_v, cudaStream_t stream);
@@ -103,5 +114,7 @@ cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *out);
 cudaError_t read_and_clear_status_bwd(uint32_t *out);
 // The one-tile forward kernel's status word (call after read_and_clear_status).
 cudaError_t read_and_clear_status_onetile(uint32_t *out);
+// The split-row forward kernel's status word (call after read_and_clear_status).
+cudaError_t read_and_clear_status_halves(uint32_t *out);
 
 }  // namespace fa

@@ -87,12 +87,15 @@ typedef enum fa_status {
  *   kv_len   const int32 [B] device pointer of key lengths, or NULL (= N).
  *   stream   cudaStream_t to enqueue on.
  *
- * Two kernels serve this call.  One gives every CTA two 128-row query tiles
- * (D <= 128); the other gives it one (any D here), for D = 256 and for grids
- * whose one-tile CTAs (2 * B * H * ceil(N/256)) fit in one wave of the GPU's
- * SMs.  The
- * environment variable FA_FWD_TILES = "1" or "2", read on every call, forces
- * one of them (D = 256 always runs the one-tile kernel).
+ * Three kernels serve this call.  One gives every CTA two 128-row query
+ * tiles (D <= 128).  One gives it one tile (any D here): D = 256, and D <= 64
+ * on grids whose one-tile CTAs (2 * B * H * ceil(N/256)) fit in one wave of
+ * the GPU's SMs.  The third gives it one tile and splits each row's keys
+ * between two softmax warpgroups, whose partial softmax states it merges at
+ * the end (D <= 128): 64 < D <= 128 with N >= 8192 or on such small grids.
+ * The environment variable FA_FWD_TILES = "1", "2" or "3", read on every
+ * call, forces one of them (D = 256 always runs the one-tile kernel).  The
+ * kernels agree to rounding, not bit for bit.
  *
  * Accumulation is fp32 (scores, running sums, O); P is rounded to bf16 for
  * the second product, and O is divided by the sum of those rounded weights
@@ -125,6 +128,13 @@ fa_status fa_fwd_f16(const void *Q, const void *K, const void *V, void *O, float
 fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, float *LSE,
                       int B, int H, int N, int D, int causal, float scale,
                       const int32_t *kv_len, void *stream);
+
+/* The forward kernel fa_fwd and fa_fwd_f16 run for these sizes on the
+ * current device: 1 = one 128-row query tile per CTA, 2 = two tiles per CTA,
+ * 3 = one tile with each row's keys split between two softmax warpgroups
+ * (FA_FWD_TILES, when set, decides as it does for those calls).  0 for a head
+ * dimension the tensor-core kernels do not take.  No device work. */
+int fa_fwd_kernel_choice(int B, int H, int N, int D);
 
 /*
  * Split-KV forward ("FlashAttention" module F08, Paper and Math: partial

@@ -155,3 +155,21 @@ def test_from_host_argument_checks(lib):
     assert call(args(Qd=P + 8)) == fa.FA_ERR_INVALID_ARG
     assert call(args(B=-1)) == fa.FA_ERR_INVALID_ARG
     assert call(args(N=0, Qh=None, Qd=None)) == fa.FA_OK                 # empty problem: nothing to do
+
+
+def test_kernel_choice(lib, monkeypatch):
+    """fa_fwd_kernel_choice answers without device work: D = 256 runs the
+    one-tile kernel, unsupported head dims give 0, long rows at D = 128 the
+    split-row kernel, many short items the two-tile kernel, and FA_FWD_TILES
+    forces a kernel except at D = 256."""
+    monkeypatch.delenv("FA_FWD_TILES", raising=False)
+    assert fa.fa_fwd_kernel_choice(1, 2, 100, 256) == 1
+    assert fa.fa_fwd_kernel_choice(1, 2, 100, 7) == 0
+    assert fa.fa_fwd_kernel_choice(1, 2, 100, 136) == 0
+    assert fa.fa_fwd_kernel_choice(1, 32, 16384, 128) == 3
+    assert fa.fa_fwd_kernel_choice(8, 16, 8191, 64) == 2
+    assert fa.fa_fwd_kernel_choice(4, 16, 4096, 128) == 2
+    for forced in ("1", "2", "3"):
+        monkeypatch.setenv("FA_FWD_TILES", forced)
+        assert fa.fa_fwd_kernel_choice(4, 16, 4096, 128) == int(forced)
+        assert fa.fa_fwd_kernel_choice(4, 16, 4096, 256) == 1

@@ -61,8 +61,8 @@ def built():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case, tiles", [("fwd", "2"), ("fwd", "1"), ("splitkv", ""), ("bwd", "")],
-                         ids=["two_tile", "one_tile", "splitkv", "bwd"])
+@pytest.mark.parametrize("case, tiles", [("fwd", "2"), ("fwd", "1"), ("fwd", "3"), ("splitkv", ""), ("bwd", "")],
+                         ids=["two_tile", "one_tile", "split_rows", "splitkv", "bwd"])
 def test_a_wait_that_runs_out_reports_a_timeout(case, tiles):
     env = dict(os.environ, FA_WAIT_LIMIT_MS="0.0002")
     env.pop("FA_FWD_TILES", None)

@@ -27,10 +27,12 @@ BF16_MAX, BF16_MEAN = 2e-2, 2e-3
 FP32_MAX = 1e-5
 
 
-@pytest.fixture(params=["1", "2"], ids=["one_tile", "two_tile"])
+@pytest.fixture(params=["1", "2", "3"], ids=["one_tile", "two_tile", "split_rows"])
 def tiles(request, monkeypatch):
     """Run a test under each tensor-core forward kernel: one or two 128-row
-    query tiles per CTA (the library reads FA_FWD_TILES on every call)."""
+    query tiles per CTA, or one tile with each row's keys split between two
+    softmax warpgroups (the library reads FA_FWD_TILES on every call; D = 256
+    always runs the one-tile kernel)."""
     monkeypatch.setenv("FA_FWD_TILES", request.param)
     return request.param
 
@@ -342,16 +344,20 @@ def test_fp32_small_cases(B, H, N, D, causal, kv_len):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_one_and_two_tile_kernels_agree(D, monkeypatch):
-    """The two forward kernels run the same per-row steps in the same key
-    order; their outputs agree to the last bf16 rounding step."""
+def test_forward_kernels_agree(D, monkeypatch):
+    """The one- and two-tile kernels run the same per-row steps in the same
+    key order; the split-row kernel merges two partial states of each row.
+    Their outputs agree to the last bf16 rounding step."""
     inp = workloads.make_case(2, 3, 700, D, dtype="bf16", causal=True, seed=D + 1, kv_len=[700, 333])
-    monkeypatch.setenv("FA_FWD_TILES", "1")
-    o1, l1 = run_gpu(inp)
-    monkeypatch.setenv("FA_FWD_TILES", "2")
-    o2, l2 = run_gpu(inp)
-    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
-    assert torch.allclose(l1, l2, rtol=0, atol=1e-4)
+    outs = {}
+    for t in ("1", "2", "3"):
+        monkeypatch.setenv("FA_FWD_TILES", t)
+        outs[t] = run_gpu(inp)
+    o1, l1 = outs["1"]
+    for t in ("2", "3"):
+        o, lse = outs[t]
+        assert (o1.float() - o.float()).abs().max().item() <= 2e-2, t
+        assert torch.allclose(l1, lse, rtol=0, atol=1e-4), t
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
@@ -564,17 +570,15 @@ def test_full_workload(name):
           f"per-head mean |dO| <= {stats[..., 1].max():.3e}, max |dLSE| {stats[..., 2].max():.3e}")
 
 
+@pytest.mark.parametrize("kernel", ["1", "2", "3"], ids=["one_tile", "two_tile", "split_rows"])
 @pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].dtype != "fp32"])
-def test_full_workload_other_kernel(name, monkeypatch):
-    """The tensor-core kernel the library does not choose for this workload
-    (one or two query tiles per CTA), forced, at full size: sampled rows
-    against the oracle."""
+def test_full_workload_every_kernel(name, kernel, monkeypatch):
+    """Each tensor-core forward kernel, forced, at full size (whichever the
+    library would choose; that one is also compared on every element by
+    test_full_workload): sampled rows against the oracle."""
     inp = workloads.make(name)
     w = inp.workload
-    items = w.B * w.H * -(-w.N // 256)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    chosen = "1" if 2 * items <= sms else "2"
-    monkeypatch.setenv("FA_FWD_TILES", "2" if chosen == "1" else "1")
+    monkeypatch.setenv("FA_FWD_TILES", kernel)
     o, lse = run_gpu(inp)
     compare(inp, o, lse, rows=sample_rows(inp, seed=w.index))
 
@@ -583,7 +587,7 @@ def test_full_workload_other_kernel(name, monkeypatch):
 def test_key_lengths_out_of_range_are_clamped(D, tiles):
     """kv_len outside [0, N] is clamped on the device: -5 acts as 0 (every
     row fully masked: exact zeros, LSE = -inf) and N + 7 as N."""
-    if D == 256 and tiles == "2":
+    if D == 256 and tiles != "1":
         pytest.skip("D = 256 always runs the one-tile kernel")
     inp = workloads.make_case(3, 2, 200, D, dtype="bf16", causal=True, seed=D + 40, kv_len=[-5, 207, 150])
     o, lse = run_gpu(inp)

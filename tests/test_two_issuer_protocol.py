@@ -16,7 +16,12 @@ softmax) refills needs a barrier of its own:
 * two-tile (D = 64): tile i's S_i(j+1) goes into its single score tile once
   the softmax of tile i holds S_i(j) in registers, P_i(j) is stored once
   O_i += P_i(j-1) V_{j-1} is done, and each K/V pair is released by a commit
-  from each thread (a barrier expecting two arrivals).
+  from each thread (a barrier expecting two arrivals);
+* split rows (one tile, each row's keys split between two softmax halves):
+  S_t goes into the single score tile once both halves hold S_{t-1} in
+  registers (s_read expects both), and half h stores P_h(j) into its P tile
+  j % 2 once O_h += P_h(j-2) V_{j-2} is done (tested early, waited for only
+  when it was not yet done).
 
 The model replays the producer, both MMA threads and the softmax warps with
 copies landing in any order and the two threads' products completing in an
@@ -24,11 +29,12 @@ arbitrary interleaving, under mbarrier semantics (a parity wait succeeds for
 any phase but the current one; a phase never takes more arrivals than it
 expects), and checks that no tile or slot is rewritten while a product or the
 softmax still needs it, that O is rescaled only after the last product into
-it is done, and that the pipeline never deadlocks.  Tests keep three
+it is done, and that the pipeline never deadlocks.  Tests keep five
 plausible mistakes pinned as failing: the one-tile softmax storing P without
 its pv_done wait (the single-thread kernel could rely on S_j's commit
-instead), the two-tile S thread not waiting for s_read, and a two-tile pair
-release that expects one arrival instead of two.
+instead), the two-tile S thread not waiting for s_read, a two-tile pair
+release that expects one arrival instead of two, a split-row s_read that
+expects one half only, and a split-row P store without its pv_done wait.
 """
 import random
 
@@ -384,3 +390,136 @@ def test_twotile_s_issue_without_s_read_is_caught():
 
 def test_twotile_pair_release_expecting_one_arrival_is_caught():
     assert _caught(lambda n, seed: _run_twotile(n, 8, seed, release_count=1), (6, 9, 16))
+
+
+# ---------------------------------------------------------------- split rows
+def _run_halves(n_kv, R, seed, s_read_count=2, skip_p_wait=False):
+    """The split-row kernel: one score tile S read by both key halves' softmax
+    warps (s_read expects both), P tiles per half and parity of the block,
+    pv_done per half and P tile, K freed by the S thread and V by the PV
+    thread.  The softmax tests pv_done early and waits only if needed."""
+    m = _Machine(seed)
+    rnd = m.rnd
+    k_full = [_Barrier() for _ in range(R)]
+    k_empty = [_Barrier() for _ in range(R)]
+    v_full = [_Barrier() for _ in range(R)]
+    v_empty = [_Barrier() for _ in range(R)]
+    s_full = _Barrier()
+    s_read = _Barrier(s_read_count)
+    p_full = [[_Barrier(), _Barrier()], [_Barrier(), _Barrier()]]      # [half][P tile]
+    pv_done = [[_Barrier(), _Barrier()], [_Barrier(), _Barrier()]]
+    st = {"k_landed": {}, "v_landed": {}, "k_busy": {}, "v_busy": {},
+          "s_tile": None, "s_unread": set(),
+          "p_tile": [[None, None], [None, None]], "p_reader": [[None, None], [None, None]],
+          "pv_last": [-1, -1]}
+
+    def producer():
+        issued = {"k": 0, "v": 0}
+
+        def load(kind):
+            t = issued[kind]
+            full, empty = (k_full, k_empty) if kind == "k" else (v_full, v_empty)
+            busy, landed = (st["k_busy"], st["k_landed"]) if kind == "k" else (st["v_busy"], st["v_landed"])
+            if t >= R:
+                while not empty[t % R].passed(((t - R) // R) & 1):
+                    yield
+            assert busy.get(t % R, 0) == 0, f"copy of {kind}{t} into a slot still read"
+            landed.pop(t % R, None)
+            full[t % R].arrive(tx=1)
+            m.copies.append((full[t % R], lambda s=t % R, t=t, landed=landed: landed.__setitem__(s, t)))
+            issued[kind] += 1
+
+        yield from load("k")
+        if n_kv > 1:
+            yield from load("k")
+        while issued["v"] < n_kv:
+            yield from load("v")
+            if issued["k"] < n_kv:
+                yield from load("k")
+            yield
+        for kind, full in (("k", k_full), ("v", v_full)):
+            for t in range(max(0, issued[kind] - R), issued[kind]):
+                while not full[t % R].passed((t // R) & 1):
+                    yield
+
+    def s_thread():
+        for t in range(n_kv):
+            while not k_full[t % R].passed((t // R) & 1):
+                yield
+            if t > 0:
+                while not s_read.passed((t - 1) & 1):
+                    yield
+            assert st["k_landed"].get(t % R) == t, f"S_{t} issued before K_{t} landed"
+            assert not st["s_unread"], f"S_{t} written before both halves read S_{t - 1}"
+            st["k_busy"][t % R] = st["k_busy"].get(t % R, 0) + 1
+
+            def done(t=t):
+                st["s_tile"] = t
+                st["s_unread"] = {0, 1}
+            q = m.queues["S"]
+            q.append(done)
+            q.append(lambda: s_full.arrive())
+            q.append(lambda s=t % R: (st["k_busy"].__setitem__(s, st["k_busy"][s] - 1), k_empty[s].arrive()))
+            yield
+
+    def pv_thread():
+        q = m.queues["PV"]
+        for j in range(n_kv):
+            buf = j & 1
+            while not v_full[j % R].passed((j // R) & 1):
+                yield
+            for h in range(2):
+                while not p_full[h][buf].passed((j >> 1) & 1):
+                    yield
+                assert st["v_landed"].get(j % R) == j, f"PV_{h}({j}) issued before V_{j} landed"
+                assert st["p_tile"][h][buf] == j, f"PV_{h}({j}) reads a P tile without P_{h}({j})"
+                st["v_busy"][j % R] = st["v_busy"].get(j % R, 0) + 1
+                st["p_reader"][h][buf] = j
+
+                def done(h=h, j=j, buf=buf):
+                    st["pv_last"][h] = j
+                    st["p_reader"][h][buf] = None
+                    st["v_busy"][j % R] -= 1
+                q.append(done)
+                q.append(lambda h=h, buf=buf: pv_done[h][buf].arrive())
+            q.append(lambda s=j % R: v_empty[s].arrive())
+            yield
+
+    def softmax(h):
+        for j in range(n_kv):
+            buf = j & 1
+            while not s_full.passed(j & 1):
+                yield
+            assert st["s_tile"] == j and h in st["s_unread"], f"half {h} of block {j} read a score tile without S_{j}"
+            p_free = j < 2 or pv_done[h][buf].passed(((j - 2) >> 1) & 1)
+            st["s_unread"].discard(h)
+            s_read.arrive()
+            yield
+            if j > 0 and rnd.random() < 0.3:       # the lazy max moves: O_h is rescaled
+                while not pv_done[h][(j - 1) & 1].passed(((j - 1) >> 1) & 1):
+                    yield
+                assert st["pv_last"][h] >= j - 1, "O_h rescaled while O_h += P V still runs"
+            if not p_free and not skip_p_wait:
+                while not pv_done[h][buf].passed(((j - 2) >> 1) & 1):
+                    yield
+            assert st["p_reader"][h][buf] is None, f"P_{h}({j}) written while a product still reads its tile"
+            st["p_tile"][h][buf] = j
+            p_full[h][buf].arrive()
+            yield
+
+    m.run([producer(), s_thread(), pv_thread(), softmax(0), softmax(1)])
+
+
+@pytest.mark.parametrize("R", [3, 4])
+@pytest.mark.parametrize("n_kv", [1, 2, 3, 4, 5, 8, 13])
+def test_split_rows_hold_their_invariants(R, n_kv):
+    for seed in range(40):
+        _run_halves(n_kv, R, seed)
+
+
+def test_split_rows_s_read_from_one_half_is_caught():
+    assert _caught(lambda n, seed: _run_halves(n, 3, seed, s_read_count=1), (3, 5, 8))
+
+
+def test_split_rows_p_store_without_its_pv_wait_is_caught():
+    assert _caught(lambda n, seed: _run_halves(n, 3, seed, skip_p_wait=True), (4, 6, 9))
