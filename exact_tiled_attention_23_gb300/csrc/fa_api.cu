@@ -311,12 +311,16 @@ int fa_fwd_kernel_choice(int B, int H, int N, int D)
 
 int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D)
 {
-    (void)D;
     if (B <= 0 || H <= 0 || N <= 0) return 1;
     const int sms = sm_count();
+    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
+    // Measured on GB300: splitting pays only at D <= 64 with long rows (N >=
+    // 4096) whose single-pass grid (2 * items one-tile CTAs) leaves SMs idle.
+    // At 64 < D <= 128 the split-row kernel runs these problems faster, and
+    // below N = 4096 the merge launch costs more than the shorter ranges save.
+    if (D > 64 || N < 4096 || 2 * items >= sms) return 1;
     // one CTA per SM (shared memory), so fill one wave without a ragged second
     // one, and keep at least two key blocks in every range
-    const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
     const int64_t blocks = ((int64_t)N + 127) / 128;
     int64_t s = items >= sms ? 1 : sms / items;
     if (s > blocks / 2) s = blocks / 2;
@@ -338,9 +342,12 @@ fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, f
     if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARG;
     if (num_splits == 0) num_splits = fa_fwd_splitkv_auto_splits(B, H, N, D);
+    if (workspace_bytes < fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits)) return FA_ERR_INVALID_ARG;
+    // One range is the whole key sequence: the single-pass kernel computes
+    // it directly, without the partial pass and the merge.
+    if (num_splits == 1) return fwd16(Q, K, V, O, LSE, B, H, N, D, causal, scale, kv_len, stream, false);
     const int64_t items = (int64_t)B * H * (((int64_t)N + 255) / 256);
     if (items * num_splits > INT32_MAX) return FA_ERR_INVALID_ARG;
-    if (workspace_bytes < fa_fwd_splitkv_workspace_bytes(B, H, N, D, num_splits)) return FA_ERR_INVALID_ARG;
 
     const int64_t BH = (int64_t)B * H;
     CUtensorMap tq, tk, tv;

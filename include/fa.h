@@ -149,6 +149,8 @@ int fa_fwd_kernel_choice(int B, int H, int N, int D);
  * Ranges that see no key have LSE_s = -inf and weight 0.
  *
  *   num_splits       1..FA_MAX_SPLITS, or 0 for fa_fwd_splitkv_auto_splits().
+ *                    With 1 split (given or chosen) the single-pass kernel
+ *                    of fa_fwd runs and the workspace is not touched.
  *   workspace        caller-owned device memory, 16-byte aligned, of at least
  *                    fa_fwd_splitkv_workspace_bytes(B,H,N,D,num_splits)
  *                    bytes; its contents on entry do not matter, it is fully
@@ -170,9 +172,11 @@ fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, f
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits);
 
 /* The split count fa_fwd_splitkv uses for num_splits = 0 on the current
- * device: as many ranges as fill one wave of CTAs (one per SM) when there are
- * fewer query items than SMs, at least two key blocks per range, at most
- * FA_MAX_SPLITS. */
+ * device.  1 unless D <= 64, N >= 4096 and fa_fwd's grid (2 * B * H *
+ * ceil(N/256) one-tile CTAs) leaves SMs idle: there, as many ranges as fill
+ * one wave of CTAs (one per SM), at least two key blocks per range, at most
+ * FA_MAX_SPLITS.  (Measured on GB300: elsewhere the split path is not faster
+ * than fa_fwd.) */
 int fa_fwd_splitkv_auto_splits(int B, int H, int N, int D);
 
 /*

@@ -173,3 +173,15 @@ def test_kernel_choice(lib, monkeypatch):
         monkeypatch.setenv("FA_FWD_TILES", forced)
         assert fa.fa_fwd_kernel_choice(4, 16, 4096, 128) == int(forced)
         assert fa.fa_fwd_kernel_choice(4, 16, 4096, 256) == 1
+
+
+def test_auto_split_count(lib):
+    """fa_fwd_splitkv_auto_splits splits only at D <= 64 with N >= 4096 and a
+    single-pass grid that leaves SMs idle (148 or 152 SMs here give the same
+    counts); otherwise 1, which runs the single-pass kernel."""
+    assert fa.fa_fwd_splitkv_auto_splits(2, 8, 1024, 64) == 1
+    assert fa.fa_fwd_splitkv_auto_splits(1, 1, 16384, 128) == 1
+    assert fa.fa_fwd_splitkv_auto_splits(1, 2, 16384, 64) == 1
+    assert fa.fa_fwd_splitkv_auto_splits(1, 1, 4096, 64) == 9
+    assert fa.fa_fwd_splitkv_auto_splits(1, 1, 16384, 64) == 2
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 1024, 64, 0) == 2 * 8 * 1024 * 65 * 4
